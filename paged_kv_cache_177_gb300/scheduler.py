@@ -1,0 +1,198 @@
+"""Iteration-level (continuous) batching on top of the block manager, and the
+static-batching comparison.
+
+Sources:
+
+* "Continuous Batching" (ultralytics.com glossary), section "Cómo funciona la
+  planificación a nivel de iteración": after each decode step the scheduler
+  returns finished sequences, frees their memory and admits queued requests
+  that fit in the KV cache; its worked example schedules eight requests on
+  four slots (static batching runs each group of four until its longest
+  member finishes; continuous batching starts the next request in the first
+  slot that frees up).
+* "Batching Continuo y PagedAttention" (cruxr.ai), sections "Batching
+  continuo (In-Flight Batching)" and "Juntándolo todo: Arquitectura de
+  vLLM": a running batch of at most B requests, a waiting queue, a block at
+  admission, a new block when the current one fills, all blocks back to the
+  pool at the end, and preemption when the pool runs dry.
+
+``IterationScheduler.step()`` yields the metadata one decode step hands to
+the device calls: the copy-on-write pairs, the append slots, and the block
+tables and context lengths of the running batch.
+"""
+from __future__ import annotations
+
+import heapq
+from collections import deque
+from dataclasses import dataclass, field
+from typing import Deque, Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+from .block_manager import BlockManager, NoFreeBlocks, blocks_needed
+
+
+def static_batching(output_lengths: Sequence[int], slots: int) -> Tuple[int, float]:
+    """Decode steps and slot occupancy when each group of ``slots`` requests
+    (in arrival order) runs until its longest member finishes."""
+    lengths = list(output_lengths)
+    steps = sum(max(lengths[i:i + slots]) for i in range(0, len(lengths), slots))
+    return steps, sum(lengths) / (steps * slots)
+
+
+def continuous_batching(output_lengths: Sequence[int], slots: int) -> Tuple[int, float]:
+    """Decode steps and slot occupancy when each queued request starts in the
+    first slot that frees up (a min-heap of the slots' free times)."""
+    free_at = [0] * slots
+    heapq.heapify(free_at)
+    for n in output_lengths:
+        start = heapq.heappop(free_at)
+        heapq.heappush(free_at, start + n)
+    steps = max(free_at)
+    return steps, sum(output_lengths) / (steps * slots)
+
+
+def utilisation_traces(output_lengths: Sequence[int], slots: int) -> Tuple[List[float], List[float]]:
+    """Per-step fraction of busy slots for static and continuous batching
+    (queue order), without padding either trace to the other's length."""
+    lengths = list(output_lengths)
+    static = []
+    for i in range(0, len(lengths), slots):
+        batch = lengths[i:i + slots]
+        for step in range(max(batch)):
+            static.append(sum(1 for n in batch if step < n) / slots)
+    cont = []
+    queue = deque(lengths)
+    active: List[int] = []
+    while active or queue:
+        while len(active) < slots and queue:
+            active.append(queue.popleft())
+        cont.append(len(active) / slots)
+        active = [r - 1 for r in active if r > 1]
+    return static, cont
+
+
+@dataclass
+class Request:
+    req_id: int
+    prompt_len: int
+    output_len: int
+    generated: int = 0
+    parent: Optional[int] = None     # fork from this request's prompt (parallel sampling)
+
+
+@dataclass
+class StepBatch:
+    """Device-call metadata of one decode step."""
+    seq_ids: List[int]
+    cow_pairs: np.ndarray        # int64 [n, 2]
+    slot_mapping: np.ndarray     # int64 [len(seq_ids)], one appended token per running sequence
+    block_tables: np.ndarray     # int32 [len(seq_ids), maxB]
+    context_lens: np.ndarray     # int32 [len(seq_ids)]
+    finished: List[int] = field(default_factory=list)
+    preempted: List[int] = field(default_factory=list)
+
+
+class IterationScheduler:
+    """Continuous batching over a paged KV pool.
+
+    Each ``step()``: admit queued requests while a slot is free and the pool
+    holds their prompt blocks; reserve one slot per running sequence (taking
+    a new block only when the last is full, copying a shared partly filled
+    block first); if the pool runs dry, preempt the most recently admitted
+    sequence (free its blocks, put it back at the head of the queue to be
+    recomputed); then retire the sequences that reached their output length.
+    """
+
+    def __init__(self, num_blocks: int, max_batch: int, block_size: int = 16,
+                 order: Optional[np.ndarray] = None):
+        self.bm = BlockManager(num_blocks, block_size, order)
+        self.max_batch = int(max_batch)
+        self.waiting: Deque[Request] = deque()
+        self.running: List[Request] = []
+        self.requests: Dict[int, Request] = {}
+        self.steps = 0
+        self.busy_slot_steps = 0
+        self.preemptions = 0
+
+    def add(self, req: Request) -> None:
+        self.requests[req.req_id] = req
+        self.waiting.append(req)
+
+    def idle(self) -> bool:
+        return not self.waiting and not self.running
+
+    def _admit(self) -> None:
+        while self.waiting and len(self.running) < self.max_batch:
+            req = self.waiting[0]
+            if req.parent is not None and self.bm.has_seq(req.parent):
+                self.bm.fork(req.parent, req.req_id)
+            else:
+                # prefill writes the prompt (and anything generated before a preemption)
+                need = blocks_needed(req.prompt_len + req.generated, self.bm.block_size)
+                if not self.bm.can_allocate(need):
+                    break
+                self.bm.allocate(req.req_id, req.prompt_len + req.generated)
+            self.waiting.popleft()
+            self.running.append(req)
+
+    def _preempt_one(self) -> Request:
+        victim = self.running.pop()
+        self.bm.free(victim.req_id)
+        self.waiting.appendleft(victim)
+        self.preemptions += 1
+        return victim
+
+    def step(self) -> Optional[StepBatch]:
+        self._admit()
+        if not self.running:
+            return None
+        pairs, slots, ids, preempted = [], [], [], []
+        i = 0
+        while i < len(self.running):
+            req = self.running[i]
+            try:
+                slot, cow = self.bm.append_slot(req.req_id)
+            except NoFreeBlocks:
+                if len(self.running) == 1:
+                    raise
+                victim = self._preempt_one()
+                preempted.append(victim.req_id)
+                if victim is req:
+                    break
+                continue
+            if cow is not None:
+                pairs.append(cow)
+            slots.append(slot)
+            ids.append(req.req_id)
+            i += 1
+        # the preempted sequences' slots were released with their blocks
+        keep = [k for k, s in enumerate(ids) if self.bm.has_seq(s)]
+        ids = [ids[k] for k in keep]
+        slots = [slots[k] for k in keep]
+        tables, lens = self.bm.tables_array(ids)
+        self.steps += 1
+        self.busy_slot_steps += len(ids)
+        finished = []
+        for req in list(self.running):
+            req.generated += 1
+            if req.generated >= req.output_len:
+                finished.append(req.req_id)
+        return StepBatch(ids, np.array(pairs, dtype=np.int64).reshape(-1, 2), np.array(slots, dtype=np.int64),
+                         tables, lens, finished, preempted)
+
+    def retire(self, batch: StepBatch) -> None:
+        """Free the blocks of the sequences the step finished."""
+        done = set(batch.finished)
+        for req in [r for r in self.running if r.req_id in done]:
+            self.bm.free(req.req_id)
+        self.running = [r for r in self.running if r.req_id not in done]
+
+    def run(self, max_steps: int = 10 ** 7) -> Tuple[int, float]:
+        """Drive until every request finished; returns (decode steps, slot occupancy)."""
+        while not self.idle() and self.steps < max_steps:
+            batch = self.step()
+            if batch is None:
+                raise RuntimeError("nothing runnable: the pool cannot hold a single waiting request")
+            self.retire(batch)
+        return self.steps, self.busy_slot_steps / (self.steps * self.max_batch)
