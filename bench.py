@@ -1,0 +1,443 @@
+"""Benchmark of one paged decode step on GB300.
+
+A step is one pass of the whole hot path over one batch of the workload:
+copy-on-write block copies (when the workload has any), the KV append of
+this step's tokens, and paged decode attention (split-context partitions and
+their log-sum-exp reduce included) for every sequence.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mha13b]
+    python bench.py --impl reference ...     # the fp64 CPU oracle on the host cores
+
+Prints one JSON line.  ``value`` is the step's algorithmic bytes (K/V read,
+q read, output written, tables, append and copy traffic) divided by the
+device time of the step, as GB/s, summed over ranks; inputs are resident in
+HBM.  ``e2e`` repeats the measurement with the per-step inputs in pinned host
+memory, copied in, and the output copied back, inside the timed region.
+Under torchrun every rank runs its own replica of the workload (weak
+scaling): the path has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from paged_kv_cache_177_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; µs per decode step"
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def describe(sp: W.WorkloadSpec) -> str:
+    if sp.lengths == "lognormal":
+        lens = f"lognormal(median {sp.len_median:g}, sigma {sp.len_sigma:g}) clipped to [{sp.len_lo}, {sp.len_hi}]"
+    elif sp.lengths == "sampling":
+        lens = (f"{sp.num_prompts} prompts x {sp.samples_per_prompt} samples, prompt {sp.prompt_len} tokens + "
+                f"suffix uniform [{sp.len_lo}, {sp.len_hi}]")
+    elif sp.lengths == "explicit":
+        lens = f"explicit lengths {list(sp.lengths_list)}"
+    else:
+        lens = f"uniform int [{sp.len_lo}, {sp.len_hi}]"
+    pool = f"pool {sp.pool_blocks} blocks" if sp.pool_blocks else f"pool {sp.pool_factor:g}x the blocks needed"
+    return (f"{sp.name}: {sp.num_seqs} seqs, {sp.num_q_heads} q / {sp.num_kv_heads} kv heads, head_dim "
+            f"{sp.head_dim}, {sp.dtype}, block 16, {lens}, shuffled {pool}")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_bytes(lay: W.Layout):
+    """Algorithmic bytes of one step, by operation."""
+    sp = lay.spec
+    eb = 2 if sp.dtype == "bf16" else 4
+    S, Hq, Hkv, D = sp.num_seqs, sp.num_q_heads, sp.num_kv_heads, sp.head_dim
+    nblk = (lay.context_lens.astype(np.int64) + 15) // 16
+    attn = lay.kv_bytes(eb) + 2 * S * Hq * D * eb + int(nblk.sum()) * 4 + S * 4
+    T = len(lay.slot_mapping)
+    append = T * Hkv * D * 2 * eb * 2 + T * 8
+    n = len(lay.cow_pairs)
+    copy = n * Hkv * 16 * D * eb * 2 * 2 + n * 16
+    return {"attention": attn, "append": append, "copy": copy, "total": attn + append + copy}
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if self.proc is None or not self.lines:
+            return None
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = max(smax, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, dist, device) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_sample(lay: W.Layout, host: dict, target_s: float):
+    """Times the oracle (fp64, all host cores) on a bounded sample of the
+    workload's sequences -- about ``target_s`` seconds of CPU work -- after
+    applying the step's copies and appends on the host.  Returns
+    (GB/s, seconds, sequences, sample bytes)."""
+    import oracle
+
+    eb = 2 if lay.spec.dtype == "bf16" else 4
+    oracle.copy_blocks(host["k_cache"], host["v_cache"], lay.cow_pairs)
+    oracle.kv_append(host["k_new"], host["v_new"], lay.slot_mapping, host["k_cache"], host["v_cache"])
+    order = np.random.default_rng(0).permutation(lay.spec.num_seqs)
+    per_token = lay.spec.num_kv_heads * lay.spec.head_dim * 2 * eb
+
+    def run(ids):
+        t0 = time.perf_counter()
+        oracle.paged_decode_attention(host["q"], host["k_cache"], host["v_cache"], lay.block_tables,
+                                      lay.context_lens, 1.0 / math.sqrt(lay.spec.head_dim), lay.spec.num_kv_heads,
+                                      seq_ids=ids, nthreads=cpu_cores())
+        return time.perf_counter() - t0
+
+    n = min(len(order), max(1, cpu_cores() // max(1, lay.spec.num_kv_heads)))
+    dt = run(order[:n])
+    while dt < target_s / 4 and n < len(order):
+        n = min(len(order), int(n * max(2.0, target_s / max(dt, 1e-3) * 0.5)))
+        dt = run(order[:n])
+    ids = order[:n]
+    nbytes = int(lay.context_lens[ids].astype(np.int64).sum()) * per_token
+    return nbytes / dt / 1e9, dt, int(n), nbytes
+
+
+def run_reference(args, rank, world, dist):
+    """The oracle, as it stands, on this host's cores: each step one bounded
+    sample of the workload (the same sequences every step)."""
+    if rank != 0:
+        return
+    import oracle
+
+    sp = W.spec(args.workload)
+    w = W.make_workload(sp, device="cpu")
+    lay = w.layout
+    host = {k: W.to_numpy(getattr(w, k)) for k in ("q", "k_cache", "v_cache", "k_new", "v_new")}
+    oracle.copy_blocks(host["k_cache"], host["v_cache"], lay.cow_pairs)
+    oracle.kv_append(host["k_new"], host["v_new"], lay.slot_mapping, host["k_cache"], host["v_cache"])
+    eb = 2 if sp.dtype == "bf16" else 4
+    per_token = sp.num_kv_heads * sp.head_dim * 2 * eb
+    order = np.random.default_rng(0).permutation(sp.num_seqs)
+    budget = args.reference_seconds / max(1, args.steps + args.warmup)
+    # size the per-step sample from one timed probe
+    n = max(1, min(len(order), cpu_cores()))
+    t0 = time.perf_counter()
+    oracle.paged_decode_attention(host["q"], host["k_cache"], host["v_cache"], lay.block_tables, lay.context_lens,
+                                  w.scale, sp.num_kv_heads, seq_ids=order[:n], nthreads=cpu_cores())
+    probe = time.perf_counter() - t0
+    n = int(max(1, min(len(order), n * budget / max(probe, 1e-3))))
+    ids = order[:n]
+    nbytes = int(lay.context_lens[ids].astype(np.int64).sum()) * per_token
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.paged_decode_attention(host["q"], host["k_cache"], host["v_cache"], lay.block_tables,
+                                      lay.context_lens, w.scale, sp.num_kv_heads, seq_ids=ids, nthreads=cpu_cores())
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    value = nbytes / t / 1e9
+    sample = (f"{n} of {sp.num_seqs} sequences ({int(lay.context_lens[ids].sum())} tokens, all heads) per step, "
+              f"fp64 C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(sp), "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local, dist):
+    from paged_kv_cache_177_gb300 import build
+    build.build_library()
+    from paged_kv_cache_177_gb300 import binding as B
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sp = W.spec(args.workload, seed=W.spec(args.workload).seed + 7919 * rank)
+    pt = args.partition_tokens if args.partition_tokens is not None else sp.partition_tokens
+    w = W.make_workload(sp, device=dev)
+    lay = w.layout
+    S, Hq, Hkv, D = sp.num_seqs, sp.num_q_heads, sp.num_kv_heads, sp.head_dim
+    maxlen = lay.max_context_len
+    nbytes = step_bytes(lay)
+    ws_bytes = B.workspace_bytes(S, Hq, Hkv, D, maxlen, pt)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(w.q)
+    stream = torch.cuda.Stream(dev)
+    has_pairs = len(lay.cow_pairs) > 0
+    split = B.partition_tokens(S, Hkv, maxlen, pt) < maxlen
+    launches_per_step = (1 if has_pairs else 0) + 1 + 1 + (1 if split else 0)
+    B.check_copy_pairs(lay.cow_pairs, lay.num_blocks)
+    # the step rewrites the same slots and blocks every time, so repeating it is idempotent
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(q, k_new, v_new, slots, tables, lens, pairs, attn_events=None):
+        if has_pairs:
+            B.copy_blocks(w.k_cache, w.v_cache, pairs, check=False, stream=stream)
+        B.kv_append(k_new, v_new, slots, w.k_cache, w.v_cache, stream=stream)
+        if attn_events is not None:
+            attn_events[0].record(stream)
+        B.paged_decode_attention(out, q, w.k_cache, w.v_cache, tables, lens, w.scale, max_context_len=maxlen,
+                                 partition_tokens=pt, workspace=ws, stream=stream)
+        if attn_events is not None:
+            attn_events[1].record(stream)
+
+    dev_inputs = (w.q, w.k_new, w.v_new, w.slot_mapping, w.block_tables, w.context_lens, w.cow_pairs)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            step(*dev_inputs)
+    torch.cuda.synchronize(dev)
+    if B.device_error(clear=True):
+        raise RuntimeError("device error word set during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    aev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        wall0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                flush.fill_(1.0)          # evict the previous step's lines from L2 (not timed)
+                ev[i][0].record(stream)
+                step(*dev_inputs, attn_events=aev[i])
+                ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    attn_ms = [a.elapsed_time(b) for a, b in aev]
+    t_step = sum(step_ms) / len(step_ms) / 1e3
+    t_attn = sum(attn_ms) / len(attn_ms) / 1e3
+    t_step_max = max_over_ranks(t_step, dist, dev)
+    total_bytes = sum_over_ranks(nbytes["total"], dist, dev)
+    value = total_bytes / t_step_max / 1e9
+
+    # ---- end to end through the C ABI: per-step inputs in pinned host memory ----
+    host_in = [t.to("cpu").pin_memory() for t in dev_inputs]
+    dev_in = [torch.empty_like(t) for t in dev_inputs]
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            flush.fill_(1.0)
+            if i >= args.warmup:
+                eev[i - args.warmup][0].record(stream)
+            for dst, src in zip(dev_in, host_in):
+                dst.copy_(src, non_blocking=True)
+            step(*dev_in)
+            host_out.copy_(out, non_blocking=True)
+            if i >= args.warmup:
+                eev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_e2e = sum(a.elapsed_time(b) for a, b in eev) / args.steps / 1e3
+    t_e2e_max = max_over_ranks(t_e2e, dist, dev)
+    e2e_value = total_bytes / t_e2e_max / 1e9
+    err = B.device_error(clear=True)
+    if err:
+        raise RuntimeError(f"device error word set during the timed steps: {err:#x}")
+
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    attn_gbs = nbytes["attention"] / t_attn / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        # the device caches already hold the step's copies and appends; the oracle
+        # re-applies them on the host (idempotent) before attending
+        host = {k: W.to_numpy(getattr(w, k)) for k in ("q", "k_cache", "v_cache", "k_new", "v_new")}
+        gbs, secs, nseq, sb = oracle_sample(lay, host, args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{nseq} of {S} sequences ({sb / 1e6:.1f} MB of K/V, all heads) in {secs:.1f} s, fp64 C "
+                         "oracle, after the step's copies and appends"}
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_step_max * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if sp.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": describe(sp),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "step": ("copy_blocks + " if has_pairs else "") + "kv_append + paged_decode_attention",
+            "partition_tokens": B.partition_tokens(S, Hkv, maxlen, pt),
+            "max_context_len": maxlen,
+            "tokens": int(lay.context_lens.sum()),
+            "step_bytes": nbytes,
+            "l2": "flushed between steps (256 MiB write, untimed) and K/V larger than L2",
+        },
+        "us_per_step": round(t_step_max * 1e6, 2),
+        "seqs_per_s": round(S * world / t_step_max, 1),
+        "pct_hbm_peak": {"measured": round(100 * value / world / peak, 2),
+                         "nominal_7.9TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2)},
+        "roofline": {
+            "kernel": "paged_decode_attention (decode_bf16_kernel" + (" + lse_reduce_kernel)" if split else ")"),
+            "bound": "hbm", "achieved": round(attn_gbs, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(attn_gbs / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+            "traffic": None, "us_per_launch": round(t_attn * 1e6, 2),
+            "bytes_per_launch": nbytes["attention"],
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(t_e2e_max * 1e3, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mha13b", choices=list(W.SPECS))
+    ap.add_argument("--partition-tokens", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-seconds", type=float, default=60.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    rank, world, local, dist = dist_setup(args)
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world, dist)
+        else:
+            run_ours(args, rank, world, local, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) PagedAttention decode library.
+ *
+ * The operations follow the pages on PagedAttention and continuous batching:
+ *
+ *  - paged_decode_attention: "PagedAttention: gestionar la KV cache como
+ *    memoria de un sistema operativo" (josueisai.com), section "Cómo funciona
+ *    por dentro" -- the attention kernel reads non-contiguous KV memory by
+ *    looking up each stretch of the sequence in its block table, scores the
+ *    query against every block's keys and takes the softmax-weighted sum of
+ *    the values.  One call performs this decode step for every sequence of a
+ *    continuously batched set ("Batching Continuo y PagedAttention",
+ *    cruxr.ai, section "Batching continuo (In-Flight Batching)").
+ *  - kv_append: same page and section -- a new token's key and value go into
+ *    the last block of the table (a new block is taken only when the last is
+ *    full; the host block manager decides, this call writes the slot).
+ *  - copy_blocks: iplexlaw.co.kr "pagedattention-vllm-kv-cache", section
+ *    "Dos respuestas a una entrada: ejemplo hipotético" -- a shared block that
+ *    still has room is copied when written while other references to it
+ *    exist (copy-on-write, "Batching Continuo y PagedAttention", section
+ *    "PagedAttention: Memoria virtual para la KV cache").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Block size P = 16 tokens ("típicamente P = 16").
+ *  - Cache layout, for one layer: k_cache and v_cache are two arrays
+ *      [num_blocks][num_kv_heads][16][head_dim]
+ *    so each (physical block, kv head) tile is one contiguous 16*head_dim run
+ *    (a block for one layer and one head stores 2*P*d_h elements, K and V).
+ *    Slot s of the pool is block s / 16, offset s % 16.
+ *  - q and out: [num_seqs][num_q_heads][head_dim]; k, v of kv_append:
+ *    [num_tokens][num_kv_heads][head_dim]. All row-major, contiguous.
+ *  - dtype: PKV_BF16 (bf16 storage, fp32 accumulation, bf16 output rounded to
+ *    nearest even) or PKV_F32 (fp32 throughout). q, caches and out share it.
+ *  - head_dim is 64 or 128; num_q_heads is a multiple of num_kv_heads and the
+ *    group size g = num_q_heads / num_kv_heads is at most 16. Query head hq
+ *    reads kv head hq / g (consecutive grouping).
+ *  - Every pointer is a DEVICE pointer unless stated otherwise, 16-byte
+ *    aligned. The caller owns all memory (including the workspace) and the
+ *    stream; the library never allocates, frees or synchronises. `stream` is a
+ *    cudaStream_t (NULL = the legacy default stream); calls are asynchronous.
+ *  - Return value: PKV_OK, or a negative status (pkv_status_string). Only
+ *    scalar arguments and pointer alignment can be checked without a
+ *    synchronisation; checks of device contents go through pkv_validate /
+ *    pkv_validate_slots, and the kernels themselves never fault on bad
+ *    contents: they skip the offending element (or read zeros) and raise a bit
+ *    in the device error word (pkv_device_error).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+#define PKV_OK 0
+#define PKV_ERR_ARG -1          /* bad scalar argument, null pointer, shape mismatch */
+#define PKV_ERR_UNSUPPORTED -2  /* head_dim, dtype or group size not supported */
+#define PKV_ERR_INDEX -3        /* index out of range (copy pairs checked on the host) */
+#define PKV_ERR_OVERLAP -4      /* copy pairs overlap: repeated destination, or a destination that is also a source */
+#define PKV_ERR_CUDA -5         /* a CUDA runtime/driver call or launch failed */
+#define PKV_ERR_WORKSPACE -6    /* workspace missing or smaller than pkv_decode_workspace_bytes */
+#define PKV_ERR_ALIGN -7        /* a pointer is not 16-byte aligned */
+
+/* Bits of the device error word. */
+#define PKV_DEVERR_BLOCK_ID 0x1u    /* a block-table entry outside [0, num_blocks): its K/V read as zeros */
+#define PKV_DEVERR_SLOT 0x2u        /* a slot >= num_blocks*16 in kv_append: that token was skipped */
+#define PKV_DEVERR_PAIR 0x4u        /* a copy pair outside [0, num_blocks): that pair was skipped */
+#define PKV_DEVERR_TIMEOUT 0x8u     /* a bounded wait inside a kernel ran out: output unspecified */
+#define PKV_DEVERR_LENGTH 0x10u     /* context_len < 0, > max_blocks_per_seq*16 or > max_context_len: clamped */
+
+/* Human-readable name of a status code (static storage). */
+const char *pkv_status_string(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int pkv_version(void);
+
+/*
+ * Effective tokens per split-context partition for a decode call (a multiple
+ * of 16). partition_tokens > 0 is returned as is (it must be a multiple of
+ * 16); 0 asks for the library's choice. A sequence of L tokens is processed
+ * as ceil(L / partition) partitions whose partial softmax statistics are
+ * merged by a log-sum-exp reduce; the result does not depend on the choice.
+ */
+int pkv_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_len, int partition_tokens);
+
+/*
+ * Bytes of device workspace paged_decode_attention needs with these
+ * arguments (0 when no sequence can span more than one partition). The
+ * workspace holds, per (sequence, query head, partition), the running max and
+ * sum of the softmax (log2 domain) and the partial output, all fp32.
+ */
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int max_context_len, int partition_tokens);
+
+/*
+ * One decode step of attention for every sequence:
+ *   out[s][hq][:] = sum_t softmax_t(scale * <q[s][hq], K_t>) V_t
+ * over the context_lens[s] tokens of sequence s, token t read from physical
+ * block block_tables[s][t / 16] at offset t % 16, kv head hq / g.
+ *
+ * block_tables: int32 [num_seqs][max_blocks_per_seq] (entries past
+ *   ceil(len/16) are never read); context_lens: int32 [num_seqs].
+ * max_context_len: host-side upper bound on every context_lens[s] (sizes the
+ *   launch); longer lengths are clamped and flagged (PKV_DEVERR_LENGTH).
+ * A context length of 0 yields a zero output row.
+ * workspace / workspace_bytes: device scratch of at least
+ *   pkv_decode_workspace_bytes(...) bytes (may be NULL when that is 0).
+ *   Concurrent calls must not share a workspace.
+ */
+int paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens, float scale,
+                           int num_kv_heads, int num_seqs, int num_q_heads, int head_dim,
+                           int max_blocks_per_seq, int num_blocks, int max_context_len, pkv_dtype dtype,
+                           int partition_tokens, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * KV append: for each token t with slot = slot_mapping[t] >= 0,
+ *   k_cache[slot / 16][h][slot % 16][:] = k[t][h][:]   (and v) for every kv head h.
+ * Negative slots are skipped (padding). Slots >= num_blocks*16 are skipped
+ * and flagged (PKV_DEVERR_SLOT). Two tokens with the same slot race.
+ * slot_mapping: int64 [num_tokens]. Bit-exact copy.
+ */
+int kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache, void *v_cache,
+              int num_tokens, int num_kv_heads, int head_dim, int num_blocks, pkv_dtype dtype, void *stream);
+
+/*
+ * Block copy (copy-on-write): for each pair i, copy physical block
+ * src_dst_pairs[i][0] onto src_dst_pairs[i][1] -- all kv heads, all 16
+ * slots -- in both k_cache and v_cache. src_dst_pairs: int64 [num_pairs][2],
+ * device. Pairs must not overlap (all destinations distinct, no destination
+ * also a source): check them on the host with pkv_check_copy_pairs. Pairs out
+ * of range are skipped and flagged (PKV_DEVERR_PAIR). Bit-exact copy.
+ */
+int copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs, int num_pairs, int num_kv_heads,
+                int head_dim, int num_blocks, pkv_dtype dtype, void *stream);
+
+/*
+ * Host-side check of copy pairs (HOST pointer, int64 [num_pairs][2]):
+ * PKV_ERR_INDEX if an id is outside [0, num_blocks), PKV_ERR_OVERLAP if a
+ * destination repeats or is also a source, else PKV_OK. No CUDA call.
+ */
+int pkv_check_copy_pairs(const int64_t *host_pairs, int num_pairs, int num_blocks);
+
+/*
+ * Device-side check of decode metadata. Clears *dev_err_word (device int32)
+ * on `stream`, then ORs into it PKV_DEVERR_BLOCK_ID for any entry
+ * block_tables[s][j], j < ceil(context_lens[s] / 16), outside [0, num_blocks),
+ * and PKV_DEVERR_LENGTH for any length < 0, > max_blocks_per_seq*16 or
+ * > max_context_len. Never traps.
+ */
+int pkv_validate(const int32_t *block_tables, const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                 int num_blocks, int max_context_len, int32_t *dev_err_word, void *stream);
+
+/* Same for a slot mapping: PKV_DEVERR_SLOT for any slot >= num_blocks*16. */
+int pkv_validate_slots(const int64_t *slot_mapping, int num_tokens, int num_blocks, int32_t *dev_err_word,
+                       void *stream);
+
+/*
+ * Reads (synchronously, on the current device) the library's device error
+ * word -- the OR of PKV_DEVERR_* bits raised by kernels since it was last
+ * cleared -- into *value, and clears it when `clear` is nonzero.
+ */
+int pkv_device_error(uint32_t *value, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,229 @@
+"""Python binding of ``libpagedkv.so`` (include/pagedkv.h) over ctypes.
+
+Argument marshalling only: shape/dtype/device checks, device pointers from
+torch tensors, the caller's current CUDA stream, and (when the caller passes
+none) a workspace tensor from torch's allocator.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback.  If the
+library is missing the import fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+from .build import LIB
+
+if not os.path.exists(LIB):
+    raise ImportError(f"{LIB} is missing: build it with paged_kv_cache_177_gb300.build.build_library() "
+                      "(or __graft_entry__.build()); there is no CPU fallback")
+
+_lib = ctypes.CDLL(LIB)
+
+PKV_F32, PKV_BF16 = 0, 1
+DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_PAIR, DEVERR_TIMEOUT, DEVERR_LENGTH = 0x1, 0x2, 0x4, 0x8, 0x10
+BLOCK_SIZE = 16
+
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+def _decl(name, restype, *argtypes):
+    fn = getattr(_lib, name)
+    fn.restype = restype
+    fn.argtypes = list(argtypes)
+    return fn
+
+
+_status_string = _decl("pkv_status_string", ctypes.c_char_p, _i)
+_version = _decl("pkv_version", _i)
+_partition_tokens = _decl("pkv_decode_partition_tokens", _i, _i, _i, _i, _i)
+_workspace_bytes = _decl("pkv_decode_workspace_bytes", _sz, _i, _i, _i, _i, _i, _i)
+_decode = _decl("paged_decode_attention", _i, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                _vp, _sz, _vp)
+_append = _decl("kv_append", _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
+_copy = _decl("copy_blocks", _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
+_check_pairs = _decl("pkv_check_copy_pairs", _i, _vp, _i, _i)
+_validate = _decl("pkv_validate", _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp)
+_validate_slots = _decl("pkv_validate_slots", _i, _vp, _i, _i, _vp, _vp)
+_device_error = _decl("pkv_device_error", _i, ctypes.POINTER(ctypes.c_uint32), _i)
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise PagedKVError(rc, what)
+
+
+def status_string(code: int) -> str:
+    return _status_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(_version())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return PKV_BF16
+    if t.dtype == torch.float32:
+        return PKV_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32")
+
+
+def _dev(*ts: torch.Tensor) -> torch.device:
+    d = ts[0].device
+    if d.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    for t in ts:
+        if t.device != d:
+            raise ValueError("all tensors must be on the same device")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    return d
+
+
+def _stream_ptr(device: torch.device, stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def partition_tokens(num_seqs: int, num_kv_heads: int, max_context_len: int, requested: int = 0) -> int:
+    return int(_partition_tokens(num_seqs, num_kv_heads, max_context_len, requested))
+
+
+def workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_context_len: int,
+                    partition_tokens: int = 0) -> int:
+    return int(_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, partition_tokens))
+
+
+def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           num_kv_heads: Optional[int] = None, *, max_context_len: Optional[int] = None,
+                           partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """out[s, hq] = softmax(scale * K_s q[s, hq]) V_s over context_lens[s] tokens
+    read through block_tables[s]; see include/pagedkv.h.
+
+    q, out: [S, Hq, D]; k_cache, v_cache: [NB, Hkv, 16, D] (bf16 or fp32,
+    all one dtype); block_tables int32 [S, maxB]; context_lens int32 [S].
+    ``max_context_len`` defaults to context_lens.max() (a device sync).
+    """
+    dev = _dev(out, q, k_cache, v_cache, block_tables, context_lens)
+    dt = _dtype_code(q)
+    if not (out.dtype == q.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("q, out and the caches must share one dtype")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    S, Hq, D = q.shape
+    NB, Hkv, P, D2 = k_cache.shape
+    if P != BLOCK_SIZE or D2 != D or v_cache.shape != k_cache.shape or out.shape != q.shape:
+        raise ValueError("expected q/out [S, Hq, D] and caches [NB, Hkv, 16, D]")
+    if num_kv_heads is not None and num_kv_heads != Hkv:
+        raise ValueError("num_kv_heads does not match the cache")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("expected block_tables [S, maxB] and context_lens [S]")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    need = workspace_bytes(S, Hq, Hkv, D, max_context_len, partition_tokens)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _dev(workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _decode(_p(out), _p(q), _p(k_cache), _p(v_cache), _p(block_tables), _p(context_lens), float(scale), Hkv, S,
+                 Hq, D, block_tables.shape[1], NB, int(max_context_len), dt, int(partition_tokens), _p(workspace),
+                 ws_bytes, _stream_ptr(dev, stream))
+    _check(rc, "paged_decode_attention")
+    return out
+
+
+def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+              v_cache: torch.Tensor, *, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """cache[slot // 16, :, slot % 16, :] = k[t] (and v) for each slot >= 0."""
+    dev = _dev(k, v, slot_mapping, k_cache, v_cache)
+    dt = _dtype_code(k)
+    if not (k.dtype == v.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("k, v and the caches must share one dtype")
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    T, Hkv, D = k.shape
+    NB, Hkv2, P, D2 = k_cache.shape
+    if v.shape != k.shape or Hkv2 != Hkv or D2 != D or P != BLOCK_SIZE or slot_mapping.shape != (T,) \
+            or v_cache.shape != k_cache.shape:
+        raise ValueError("expected k, v [T, Hkv, D], slot_mapping [T], caches [NB, Hkv, 16, D]")
+    _check(_append(_p(k), _p(v), _p(slot_mapping), _p(k_cache), _p(v_cache), T, Hkv, D, NB, dt,
+                   _stream_ptr(dev, stream)), "kv_append")
+
+
+def check_copy_pairs(pairs, num_blocks: int) -> None:
+    """Host-side range/overlap check of (src, dst) pairs; raises PagedKVError."""
+    arr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    _check(_check_pairs(arr.ctypes.data if arr.size else None, arr.shape[0], int(num_blocks)), "copy_blocks pairs")
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: torch.Tensor, *,
+                host_pairs=None, check: bool = True, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copies whole blocks src -> dst of both caches.  ``src_dst_pairs``:
+    int64 [n, 2] on the device.  With ``check`` the pairs are range- and
+    overlap-checked on the host first (``host_pairs`` if given, else a copy
+    of the device pairs, which synchronises)."""
+    dev = _dev(k_cache, v_cache, src_dst_pairs)
+    dt = _dtype_code(k_cache)
+    if src_dst_pairs.dtype != torch.int64:
+        raise TypeError("src_dst_pairs must be int64")
+    n = src_dst_pairs.numel() // 2
+    if src_dst_pairs.numel() != 2 * n:
+        raise ValueError("src_dst_pairs must be [n, 2]")
+    NB, Hkv, P, D = k_cache.shape
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype or P != BLOCK_SIZE:
+        raise ValueError("caches must be [NB, Hkv, 16, D] of one dtype")
+    if check:
+        check_copy_pairs(host_pairs if host_pairs is not None else src_dst_pairs.cpu().numpy(), NB)
+    _check(_copy(_p(k_cache), _p(v_cache), _p(src_dst_pairs) if n else None, n, Hkv, D, NB, dt,
+                 _stream_ptr(dev, stream)), "copy_blocks")
+
+
+def validate(block_tables: torch.Tensor, context_lens: torch.Tensor, num_blocks: int, max_context_len: int,
+             err_word: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Device-side range check of decode metadata; returns the int32 error word tensor."""
+    dev = _dev(block_tables, context_lens)
+    if err_word is None:
+        err_word = torch.empty(1, dtype=torch.int32, device=dev)
+    S = context_lens.shape[0]
+    _check(_validate(_p(block_tables), _p(context_lens), S, block_tables.shape[1], int(num_blocks),
+                     int(max_context_len), _p(err_word), _stream_ptr(dev, stream)), "pkv_validate")
+    return err_word
+
+
+def validate_slots(slot_mapping: torch.Tensor, num_blocks: int, err_word: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    dev = _dev(slot_mapping)
+    if err_word is None:
+        err_word = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(_validate_slots(_p(slot_mapping), slot_mapping.numel(), int(num_blocks), _p(err_word),
+                           _stream_ptr(dev, stream)), "pkv_validate_slots")
+    return err_word
+
+
+def device_error(clear: bool = True) -> int:
+    """The library's device error word on the current device (synchronous)."""
+    v = ctypes.c_uint32(0)
+    _check(_device_error(ctypes.byref(v), 1 if clear else 0), "pkv_device_error")
+    return int(v.value)
+
+
+def raw_library() -> ctypes.CDLL:
+    """The loaded ctypes library (for callers that pass raw pointers)."""
+    return _lib

@@ -1,0 +1,298 @@
+// pkv.cu -- host side of the C ABI declared in include/pagedkv.h: argument
+// checks, split-context planning, TMA descriptor encoding and launches.
+// The library never allocates device memory and never synchronises, except
+// pkv_device_error(), which is documented as synchronous.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <unordered_set>
+
+#include "pagedkv.h"
+#include "pkv_kernels.cuh"
+
+namespace {
+
+constexpr int kVersion = 100;          // 0.1.0
+constexpr int kDefaultPartition = 512; // tokens per split-context partition (32 blocks)
+constexpr int kMaxParts = 8192;        // partitions per sequence the reduce kernel handles
+constexpr int kNstage = 8;
+constexpr int kNcw = 4;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(pkv_dtype dt) { return dt == PKV_BF16 ? 2 : 4; }
+
+bool dtype_ok(pkv_dtype dt) { return dt == PKV_BF16 || dt == PKV_F32; }
+
+int check_launch() {
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// cuTensorMapEncodeTiled from the driver, fetched through the runtime so the
+// library does not link libcuda directly.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 2-D view of a cache as rows of head_dim bf16: row = (block * Hkv + head) * 16
+// + slot. Box = 16 rows x 64 elements (one 128-byte swizzle span), so a
+// (block, head) tile of head_dim 128 is two boxes.
+int encode_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int num_kv_heads, int head_dim) {
+    auto fn = encode_fn();
+    if (!fn) return PKV_ERR_CUDA;
+    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)num_blocks * num_kv_heads * 16};
+    cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+    cuuint32_t box[2] = {64, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(cache), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int max_parts_for(int max_context_len, int part_tokens) {
+    if (max_context_len <= 0) return 1;
+    return (max_context_len + part_tokens - 1) / part_tokens;
+}
+
+template <int D, int NT>
+int launch_bf16(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, dim3 grid,
+                cudaStream_t st) {
+    using C = pkv::Bf16Cfg<D, NT, kNstage, kNcw>;
+    auto kern = pkv::decode_bf16_kernel<D, NT, kNstage, kNcw>;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (configured_device != dev) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured_device = dev;
+    }
+    kern<<<grid, C::kThreads, C::kSmem, st>>>(tmk, tmv, p);
+    return check_launch();
+}
+
+template <int D>
+int launch_f32(const pkv::DecodeParams &p, dim3 grid, cudaStream_t st) {
+    const size_t smem = (size_t)kNcw * p.group * (D + 2) * sizeof(float);
+    pkv::decode_f32_kernel<D, kNcw><<<grid, kNcw * 32, smem, st>>>(p);
+    return check_launch();
+}
+
+template <int D>
+int launch_reduce(const pkv::DecodeParams &p, pkv_dtype dt, cudaStream_t st) {
+    dim3 grid(p.num_q_heads, p.num_seqs);
+    const size_t smem = (32 + (size_t)p.max_parts) * sizeof(float);
+    if (dt == PKV_BF16)
+        pkv::lse_reduce_kernel<__nv_bfloat16, D><<<grid, D, smem, st>>>(p);
+    else
+        pkv::lse_reduce_kernel<float, D><<<grid, D, smem, st>>>(p);
+    return check_launch();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pkv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_ARG: return "bad argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported head_dim, dtype or group size";
+        case PKV_ERR_INDEX: return "index out of range";
+        case PKV_ERR_OVERLAP: return "copy pairs overlap";
+        case PKV_ERR_CUDA: return "CUDA error";
+        case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+        case PKV_ERR_ALIGN: return "pointer not 16-byte aligned";
+        default: return "unknown status";
+    }
+}
+
+int pkv_version(void) { return kVersion; }
+
+int pkv_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_len, int partition_tokens) {
+    (void)num_seqs;
+    (void)num_kv_heads;
+    (void)max_context_len;
+    if (partition_tokens > 0) return partition_tokens;
+    return kDefaultPartition;
+}
+
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
+                                  int partition_tokens) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+    const int pt = pkv_decode_partition_tokens(num_seqs, num_kv_heads, max_context_len, partition_tokens);
+    if (pt <= 0 || pt % 16 != 0) return 0;
+    const int mp = max_parts_for(max_context_len, pt);
+    if (mp <= 1) return 0;
+    return (size_t)num_seqs * num_q_heads * mp * (2 + (size_t)head_dim) * sizeof(float);
+}
+
+int paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens, float scale, int num_kv_heads,
+                           int num_seqs, int num_q_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
+                           int max_context_len, pkv_dtype dtype, int partition_tokens, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+        max_context_len < 0 || partition_tokens < 0)
+        return PKV_ERR_ARG;
+    if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0) return PKV_ERR_ARG;
+    const int g = num_q_heads / num_kv_heads;
+    if (g > 16) return PKV_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return PKV_ERR_ARG;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)num_blocks * num_kv_heads * 16 >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+    const int pt = pkv_decode_partition_tokens(num_seqs, num_kv_heads, max_context_len, partition_tokens);
+    if (pt % 16 != 0) return PKV_ERR_ARG;
+    const int mp = max_parts_for(max_context_len, pt);
+    if (mp > kMaxParts) return PKV_ERR_UNSUPPORTED;
+    const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                                                   partition_tokens);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PKV_ERR_WORKSPACE;
+
+    pkv::DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.ws_ml = static_cast<float *>(workspace);
+    p.ws_o = need ? static_cast<float *>(workspace) + (size_t)num_seqs * num_q_heads * mp * 2 : nullptr;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = g;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.max_context_len = max_context_len;
+    p.part_blocks = pt / 16;
+    p.max_parts = mp;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    dim3 grid(mp, num_kv_heads, num_seqs);
+    int rc;
+    if (dtype == PKV_BF16) {
+        alignas(64) CUtensorMap tmk, tmv;
+        if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
+        if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
+        if (head_dim == 128)
+            rc = g <= 8 ? launch_bf16<128, 1>(tmk, tmv, p, grid, st) : launch_bf16<128, 2>(tmk, tmv, p, grid, st);
+        else
+            rc = g <= 8 ? launch_bf16<64, 1>(tmk, tmv, p, grid, st) : launch_bf16<64, 2>(tmk, tmv, p, grid, st);
+    } else {
+        rc = head_dim == 128 ? launch_f32<128>(p, grid, st) : launch_f32<64>(p, grid, st);
+    }
+    if (rc != PKV_OK) return rc;
+    if (mp > 1) rc = head_dim == 128 ? launch_reduce<128>(p, dtype, st) : launch_reduce<64>(p, dtype, st);
+    return rc;
+}
+
+int kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache, void *v_cache, int num_tokens,
+              int num_kv_heads, int head_dim, int num_blocks, pkv_dtype dtype, void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_ARG;
+    if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+    const int vec_per_row = head_dim * elem_bytes(dtype) / 16;
+    pkv::kv_append_kernel<<<num_tokens, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, static_cast<uint4 *>(k_cache),
+        static_cast<uint4 *>(v_cache), num_kv_heads, vec_per_row, num_blocks);
+    return check_launch();
+}
+
+int copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs, int num_pairs, int num_kv_heads,
+                int head_dim, int num_blocks, pkv_dtype dtype, void *stream) {
+    if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_ARG;
+    if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PKV_OK;
+    if (num_pairs > 65535) return PKV_ERR_UNSUPPORTED;
+    if (!k_cache || !v_cache || !src_dst_pairs) return PKV_ERR_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+    const int64_t vec_per_block = (int64_t)num_kv_heads * 16 * head_dim * elem_bytes(dtype) / 16;
+    const int threads = 256;
+    int64_t chunks = (vec_per_block + threads * 4 - 1) / (threads * 4);
+    if (chunks > 1024) chunks = 1024;
+    dim3 grid((unsigned)chunks, num_pairs, 2);
+    pkv::copy_blocks_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src_dst_pairs, num_blocks, vec_per_block);
+    return check_launch();
+}
+
+int pkv_check_copy_pairs(const int64_t *host_pairs, int num_pairs, int num_blocks) {
+    if (num_pairs < 0 || num_blocks <= 0) return PKV_ERR_ARG;
+    if (num_pairs > 0 && !host_pairs) return PKV_ERR_ARG;
+    std::unordered_set<int64_t> srcs, dsts;
+    for (int i = 0; i < num_pairs; ++i) {
+        const int64_t s = host_pairs[2 * i], d = host_pairs[2 * i + 1];
+        if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) return PKV_ERR_INDEX;
+        srcs.insert(s);
+        if (!dsts.insert(d).second) return PKV_ERR_OVERLAP;
+    }
+    for (int64_t d : dsts)
+        if (srcs.count(d)) return PKV_ERR_OVERLAP;
+    return PKV_OK;
+}
+
+int pkv_validate(const int32_t *block_tables, const int32_t *context_lens, int num_seqs, int max_blocks_per_seq,
+                 int num_blocks, int max_context_len, int32_t *dev_err_word, void *stream) {
+    if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 || !dev_err_word)
+        return PKV_ERR_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(dev_err_word, 0, sizeof(int32_t), st) != cudaSuccess) return PKV_ERR_CUDA;
+    if (num_seqs == 0) return PKV_OK;
+    if (!block_tables || !context_lens) return PKV_ERR_ARG;
+    pkv::validate_tables_kernel<<<num_seqs, 128, 0, st>>>(block_tables, context_lens, max_blocks_per_seq, num_blocks,
+                                                          max_context_len, dev_err_word);
+    return check_launch();
+}
+
+int pkv_validate_slots(const int64_t *slot_mapping, int num_tokens, int num_blocks, int32_t *dev_err_word,
+                       void *stream) {
+    if (num_tokens < 0 || num_blocks <= 0 || !dev_err_word) return PKV_ERR_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(dev_err_word, 0, sizeof(int32_t), st) != cudaSuccess) return PKV_ERR_CUDA;
+    if (num_tokens == 0) return PKV_OK;
+    if (!slot_mapping) return PKV_ERR_ARG;
+    pkv::validate_slots_kernel<<<(num_tokens + 255) / 256, 256, 0, st>>>(slot_mapping, num_tokens, num_blocks,
+                                                                        dev_err_word);
+    return check_launch();
+}
+
+int pkv_device_error(uint32_t *value, int clear) {
+    if (!value) return PKV_ERR_ARG;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, pkv::g_dev_error, sizeof(v)) != cudaSuccess) return PKV_ERR_CUDA;
+    *value = v;
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(pkv::g_dev_error, &zero, sizeof(zero)) != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,593 @@
+// pkv_kernels.cuh -- device code of the PagedAttention decode library.
+//
+// K1 decode_bf16_kernel   block-table gather (TMA) + QK^T + online softmax + PV on tensor cores
+// K1 decode_f32_kernel    the same step in fp32 on the CUDA cores (exact-precision path)
+// K2 lse_reduce_kernel    merges split-context partitions with a log-sum-exp reduce
+// K3 kv_append_kernel     slot-mapped write of new tokens' K/V
+// K4 copy_blocks_kernel   whole-block copy for copy-on-write
+// K5 validate_*_kernel    device-side range checks of the metadata
+//
+// The method ("PagedAttention: gestionar la KV cache como memoria de un
+// sistema operativo", josueisai.com, section "Cómo funciona por dentro"):
+// attention walks a sequence's block table in logical order, reading each
+// physical block's keys and values, and returns the softmax-weighted sum of
+// the values. Blocks hold 16 tokens ("Batching Continuo y PagedAttention",
+// cruxr.ai, section "PagedAttention: Memoria virtual para la KV cache").
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+#include "pkv_ptx.cuh"
+
+namespace pkv {
+
+constexpr int kBlock = 16;  // tokens per physical block
+
+// Device error word (PKV_DEVERR_* bits), read back by pkv_device_error().
+__device__ unsigned int g_dev_error = 0;
+
+__device__ __forceinline__ void raise_error(unsigned int bits) { atomicOr(&g_dev_error, bits); }
+
+struct DecodeParams {
+    void *out;                    // [S][Hq][D]
+    const void *q;                // [S][Hq][D]
+    const void *k_cache;          // [NB][Hkv][16][D] (fp32 path; bf16 path reads through tensor maps)
+    const void *v_cache;
+    const int32_t *block_tables;  // [S][maxB]
+    const int32_t *context_lens;  // [S]
+    float *ws_ml;                 // [S][Hq][max_parts][2]: running max (log2 domain), sum
+    float *ws_o;                  // [S][Hq][max_parts][D]: partition output, normalised by its own sum
+    float scale_log2;             // scale * log2(e): scores are kept in the log2 domain
+    int num_seqs, num_q_heads, num_kv_heads, group;
+    int max_blocks_per_seq, num_blocks, max_context_len;
+    int part_blocks;              // blocks per split-context partition
+    int max_parts;                // partitions allotted per (sequence, head) in the workspace
+};
+
+// A sequence's usable length: negative lengths and lengths past the table or
+// past max_context_len are clamped (and flagged by thread 0 of one CTA).
+__device__ __forceinline__ int seq_len(const DecodeParams &p, int s, bool flag) {
+    int len = __ldg(p.context_lens + s);
+    const int cap = min(p.max_blocks_per_seq * kBlock, p.max_context_len);
+    if (len < 0 || len > cap) {
+        if (flag) raise_error(PKV_DEVERR_LENGTH);
+        len = len < 0 ? 0 : cap;
+    }
+    return len;
+}
+
+// =====================================================================================
+// K1 (bf16): one CTA per (split-context partition, kv head, sequence).
+//
+// Warp NCW is the producer: it reads the partition's block ids from the table
+// 32 at a time and, for each block, issues TMA loads of the (block, kv head)
+// K and V tiles -- [16 tokens][D] each, contiguous in HBM -- into a ring of
+// NSTAGE shared-memory stages (128-byte swizzle, so fragment loads are free
+// of bank conflicts). Warps 0..NCW-1 consume blocks round-robin; each keeps
+// its own online-softmax state for the g query heads of the group:
+//   S^T[16 tok x 8 heads]  = K[16 x D] . Q^T[D x 8]       (mma m16n8k16, bf16)
+//   m' = max(m, max_t s_t);  p_t = 2^(s_t - m');  l = l 2^(m - m') + sum_t p_t
+//   O^T[D x 8 heads]      = O^T 2^(m - m') + V^T[D x 16] . P^T[16 x 8]
+// The query heads of a GQA group share every K/V tile: the tile is read from
+// HBM once per group, and the group (padded to 8 or 16) is the MMA's N.
+// At the end the consumer warps merge their states through shared memory and
+// either write the final output (single-partition sequence) or the
+// partition's (max, sum, output) for the log-sum-exp reduce.
+// =====================================================================================
+template <int D, int NT, int NSTAGE, int NCW>
+struct Bf16Cfg {
+    static constexpr int kSub = D / 64;                 // 128-byte-wide sub-tiles per tile
+    static constexpr int kSubBytes = kBlock * 128;      // 2 KiB: 16 rows of 64 bf16
+    static constexpr int kTile = kBlock * D * 2;        // one (block, head) tile of K or V
+    static constexpr int kStage = 2 * kTile;            // K tile + V tile
+    static constexpr int kSteps = D / 16;               // k-steps of QK^T, m-tiles of PV
+    static constexpr int kThreads = (NCW + 1) * 32;
+    static constexpr int kHeads = NT * 8;               // padded group width (MMA N)
+    static constexpr int kMergeStride = D + 4;          // padded row of the merge buffer
+    static constexpr int kMergeBytes = NCW * kHeads * (2 + kMergeStride) * 4;
+    static constexpr int kBarOffset = NSTAGE * kStage;
+    static constexpr int kSmem = kBarOffset + 2 * NSTAGE * 8 + 1024;  // + slack for 1 KiB alignment
+    static_assert(kMergeBytes <= kBarOffset, "merge buffer must fit in the stage ring");
+    static_assert(NSTAGE % NCW == 0, "each stage is always consumed by the same warp");
+};
+
+template <int D, int NT, int NSTAGE, int NCW>
+__global__ void __launch_bounds__((NCW + 1) * 32)
+    decode_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                       const DecodeParams p) {
+    using C = Bf16Cfg<D, NT, NSTAGE, NCW>;
+    extern __shared__ uint8_t smem_raw[];
+
+    const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = p.group;
+    const int len = seq_len(p, s, tid == 0 && part == 0 && h == 0);
+    const int nblk = (len + kBlock - 1) / kBlock;
+    const int npart = (nblk + p.part_blocks - 1) / p.part_blocks;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+
+    if (len == 0) {  // empty context: zero output rows
+        if (part == 0) {
+            __nv_bfloat16 *o = out + ((size_t)s * p.num_q_heads + (size_t)h * g) * D;
+            for (int i = tid; i < g * D; i += C::kThreads) o[i] = __float2bfloat16_rn(0.f);
+        }
+        return;
+    }
+    if (part >= npart) return;
+
+    const int b_begin = part * p.part_blocks;
+    const int nb = min(nblk - b_begin, p.part_blocks);
+    const int last_valid = len - (nblk - 1) * kBlock;  // tokens in the sequence's last block
+
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + C::kBarOffset);
+    uint64_t *empty = full + NSTAGE;
+    if (tid == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == NCW) {
+        // ------------------------------ producer ------------------------------
+        const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks_per_seq + b_begin;
+        bool ok = true;
+        for (int jb = 0; jb < nb && ok; jb += 32) {
+            const int mine = (jb + lane < nb) ? __ldg(bt + jb + lane) : 0;
+            const int cnt = min(32, nb - jb);
+            for (int i = 0; i < cnt; ++i) {
+                const int pb = __shfl_sync(0xffffffffu, mine, i);
+                const int j = jb + i;
+                if (lane == 0) {
+                    const int st = j % NSTAGE;
+                    if (j >= NSTAGE && !mbar_wait(&empty[st], ((j / NSTAGE) - 1) & 1)) {
+                        raise_error(PKV_DEVERR_TIMEOUT);
+                        ok = false;
+                    }
+                    if (ok) {
+                        int y;
+                        if (pb < 0 || pb >= p.num_blocks) {
+                            raise_error(PKV_DEVERR_BLOCK_ID);
+                            y = -kBlock;  // wholly outside the tensor: the tile reads as zeros
+                        } else {
+                            y = (pb * p.num_kv_heads + h) * kBlock;
+                        }
+                        mbar_arrive_expect_tx(&full[st], C::kStage);
+                        uint8_t *sk = base + st * C::kStage;
+#pragma unroll
+                        for (int u = 0; u < C::kSub; ++u) tma_load_2d(sk + u * C::kSubBytes, &tmk, u * 64, y, &full[st]);
+#pragma unroll
+                        for (int u = 0; u < C::kSub; ++u)
+                            tma_load_2d(sk + C::kTile + u * C::kSubBytes, &tmv, u * 64, y, &full[st]);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+        }
+        return;
+    }
+
+    // ------------------------------ consumers ------------------------------
+    const int gq = lane >> 2, t4 = lane & 3;
+    // Q^T as the B operand of QK^T: b0 = q[head gq][16kk + 2t4 .. +1], b1 = same + 8.
+    uint32_t qf[C::kSteps][NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hl = nt * 8 + gq;
+        const bool hv = hl < g;
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+            static_cast<const __nv_bfloat16 *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)h * g + (hv ? hl : 0)) * D);
+#pragma unroll
+        for (int kk = 0; kk < C::kSteps; ++kk) {
+            qf[kk][nt][0] = hv ? __ldg(qrow + (16 * kk + 2 * t4) / 2) : 0u;
+            qf[kk][nt][1] = hv ? __ldg(qrow + (16 * kk + 8 + 2 * t4) / 2) : 0u;
+        }
+    }
+
+    float m_run[NT][2], l_run[NT][2];
+    float acc[C::kSteps][NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        m_run[nt][0] = m_run[nt][1] = -INFINITY;
+        l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < C::kSteps; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+    }
+
+    const int mi = lane >> 3, r8 = lane & 7;
+    for (int j = warp; j < nb; j += NCW) {
+        const int st = j % NSTAGE;
+        if (!mbar_wait(&full[st], (j / NSTAGE) & 1)) {
+            raise_error(PKV_DEVERR_TIMEOUT);
+            break;
+        }
+        const uint32_t sk = smem_u32(base + st * C::kStage);
+        const uint32_t sv = sk + C::kTile;
+        const int valid = (b_begin + j == nblk - 1) ? last_valid : kBlock;
+
+        // S^T = K . Q^T  (rows: the block's 16 tokens; columns: the group's heads)
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < C::kSteps; ++kk) {
+            const int u = kk >> 2;
+            const int row = r8 + (mi & 1) * 8;
+            const int chunk = (kk & 3) * 2 + (mi >> 1);
+            uint32_t a[4];
+            ldsm_x4(sk + u * C::kSubBytes + row * 128 + ((chunk ^ (row & 7)) << 4), a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], a, qf[kk][nt][0], qf[kk][nt][1]);
+        }
+
+        // online softmax (log2 domain); tokens past the sequence end get -inf
+        const bool v0 = gq < valid, v1 = gq + 8 < valid;
+        uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const float x0 = v0 ? sc[nt][0] * p.scale_log2 : -INFINITY;
+            const float x1 = v0 ? sc[nt][1] * p.scale_log2 : -INFINITY;
+            const float x2 = v1 ? sc[nt][2] * p.scale_log2 : -INFINITY;
+            const float x3 = v1 ? sc[nt][3] * p.scale_log2 : -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
+            const float al0 = ex2_approx(m_run[nt][0] - mn0), al1 = ex2_approx(m_run[nt][1] - mn1);
+            m_run[nt][0] = mn0;
+            m_run[nt][1] = mn1;
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(ex2_approx(x0 - mn0), ex2_approx(x1 - mn1));
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(ex2_approx(x2 - mn0), ex2_approx(x3 - mn1));
+            const float2 flo = __bfloat1622float2(lo), fhi = __bfloat1622float2(hi);
+            // the sum uses the rounded weights the PV product uses, so they stay normalised
+            l_run[nt][0] = l_run[nt][0] * al0 + (flo.x + fhi.x);
+            l_run[nt][1] = l_run[nt][1] * al1 + (flo.y + fhi.y);
+#pragma unroll
+            for (int mt = 0; mt < C::kSteps; ++mt) {
+                acc[mt][nt][0] *= al0;
+                acc[mt][nt][1] *= al1;
+                acc[mt][nt][2] *= al0;
+                acc[mt][nt][3] *= al1;
+            }
+            // P^T as the B operand of PV: transpose the (token x head) 8x8 quads
+            pb0[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&lo));
+            pb1[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&hi));
+        }
+
+        // V rows past the sequence end may hold anything (even NaN): zero them so
+        // that 0-weight * V cannot poison the product
+        if (valid < kBlock) {
+            const int nrow = kBlock - valid;
+            for (int i = lane; i < nrow * 8 * C::kSub; i += 32) {
+                const int u = i / (nrow * 8), rem = i % (nrow * 8);
+                st_shared_zero16(sv + u * C::kSubBytes + (valid + rem / 8) * 128 + (rem % 8) * 16);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+
+        // O^T += V^T . P^T  (rows: head-dim, 16 per m-tile; columns: heads)
+#pragma unroll
+        for (int mt = 0; mt < C::kSteps; ++mt) {
+            const int u = mt >> 2;
+            const int row = r8 + (mi >> 1) * 8;
+            const int chunk = (mt & 3) * 2 + (mi & 1);
+            uint32_t a[4];
+            ldsm_x4_trans(sv + u * C::kSubBytes + row * 128 + ((chunk ^ (row & 7)) << 4), a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a, pb0[nt], pb1[nt]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    // ---------------- merge the consumer warps' states ----------------
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) l_run[nt][c] += __shfl_xor_sync(0xffffffffu, l_run[nt][c], o);
+
+    named_barrier_sync(1, NCW * 32);  // every consumer is done with the stage ring
+    float *mml = reinterpret_cast<float *>(base);                    // [NCW][kHeads][2]
+    float *macc = mml + NCW * C::kHeads * 2;                         // [NCW][kHeads][kMergeStride]
+    if (gq == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int head = nt * 8 + 2 * t4 + c;
+                mml[(warp * C::kHeads + head) * 2 + 0] = m_run[nt][c];
+                mml[(warp * C::kHeads + head) * 2 + 1] = l_run[nt][c];
+            }
+    }
+#pragma unroll
+    for (int mt = 0; mt < C::kSteps; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int head = nt * 8 + 2 * t4 + (e & 1);
+                const int d = 16 * mt + gq + (e >> 1) * 8;
+                macc[(warp * C::kHeads + head) * C::kMergeStride + d] = acc[mt][nt][e];
+            }
+    named_barrier_sync(1, NCW * 32);
+
+    for (int idx = tid; idx < g * D; idx += NCW * 32) {
+        const int head = idx / D, d = idx - head * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, mml[(w * C::kHeads + head) * 2]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+            const float mw = mml[(w * C::kHeads + head) * 2];
+            const float f = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
+            L += mml[(w * C::kHeads + head) * 2 + 1] * f;
+            O += macc[(w * C::kHeads + head) * C::kMergeStride + d] * f;
+        }
+        const float o = O / L;
+        const size_t orow = (size_t)s * p.num_q_heads + (size_t)h * g + head;
+        if (npart == 1) {
+            out[orow * D + d] = __float2bfloat16_rn(o);
+        } else {
+            const size_t r = orow * p.max_parts + part;
+            p.ws_o[r * D + d] = o;
+            if (d == 0) {
+                p.ws_ml[r * 2 + 0] = M;
+                p.ws_ml[r * 2 + 1] = L;
+            }
+        }
+    }
+}
+
+// =====================================================================================
+// K1 (fp32): same decomposition on the CUDA cores, for fp32 caches where the
+// result must hold to ~1e-5. One CTA per (partition, kv head, sequence); warp w
+// takes blocks w, w+NCW, ...; lane l owns head-dim elements l, l+32, ...
+// Each token: x = scale log2(e) <q, K_t> (warp sum), then the online update
+//   m' = max(m, x), l = l 2^(m-m') + 2^(x-m'), acc = acc 2^(m-m') + 2^(x-m') V_t.
+// =====================================================================================
+template <int D, int NCW>
+__global__ void __launch_bounds__(NCW * 32) decode_f32_kernel(const DecodeParams p) {
+    constexpr int PER = D / 32;
+    extern __shared__ float fsm[];  // merge buffer: [NCW][g][D + 2]
+    const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = p.group;
+    const int len = seq_len(p, s, tid == 0 && part == 0 && h == 0);
+    const int nblk = (len + kBlock - 1) / kBlock;
+    const int npart = (nblk + p.part_blocks - 1) / p.part_blocks;
+    float *out = static_cast<float *>(p.out);
+    if (len == 0) {
+        if (part == 0) {
+            float *o = out + ((size_t)s * p.num_q_heads + (size_t)h * g) * D;
+            for (int i = tid; i < g * D; i += NCW * 32) o[i] = 0.f;
+        }
+        return;
+    }
+    if (part >= npart) return;
+    const int b_begin = part * p.part_blocks;
+    const int nb = min(nblk - b_begin, p.part_blocks);
+    const int last_valid = len - (nblk - 1) * kBlock;
+    const float *kc = static_cast<const float *>(p.k_cache);
+    const float *vc = static_cast<const float *>(p.v_cache);
+    const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks_per_seq + b_begin;
+
+    for (int n = 0; n < g; ++n) {
+        const float *qrow = static_cast<const float *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)h * g + n) * D;
+        float qv[PER], acc[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            qv[i] = __ldg(qrow + lane + 32 * i);
+            acc[i] = 0.f;
+        }
+        float m = -INFINITY, l = 0.f;
+        for (int j = warp; j < nb; j += NCW) {
+            const int pb = __ldg(bt + j);
+            const bool bad = pb < 0 || pb >= p.num_blocks;
+            if (bad && lane == 0 && n == 0) raise_error(PKV_DEVERR_BLOCK_ID);
+            const int valid = (b_begin + j == nblk - 1) ? last_valid : kBlock;
+            const size_t tile = bad ? 0 : ((size_t)pb * p.num_kv_heads + h) * kBlock * D;
+            for (int t = 0; t < valid; ++t) {
+                float dot = 0.f;
+                float vv[PER];
+#pragma unroll
+                for (int i = 0; i < PER; ++i) {
+                    const float kx = bad ? 0.f : __ldg(kc + tile + (size_t)t * D + lane + 32 * i);
+                    vv[i] = bad ? 0.f : __ldg(vc + tile + (size_t)t * D + lane + 32 * i);
+                    dot = fmaf(qv[i], kx, dot);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                const float x = dot * p.scale_log2;
+                const float mn = fmaxf(m, x);
+                const float al = exp2f(m - mn);
+                const float pw = exp2f(x - mn);
+                l = l * al + pw;
+#pragma unroll
+                for (int i = 0; i < PER; ++i) acc[i] = fmaf(acc[i], al, pw * vv[i]);
+                m = mn;
+            }
+        }
+        float *row = fsm + ((size_t)warp * g + n) * (D + 2);
+#pragma unroll
+        for (int i = 0; i < PER; ++i) row[2 + lane + 32 * i] = acc[i];
+        if (lane == 0) {
+            row[0] = m;
+            row[1] = l;
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < g * D; idx += NCW * 32) {
+        const int n = idx / D, d = idx - n * D;
+        float M = -INFINITY;
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, fsm[((size_t)w * g + n) * (D + 2)]);
+        float L = 0.f, O = 0.f;
+        for (int w = 0; w < NCW; ++w) {
+            const float *row = fsm + ((size_t)w * g + n) * (D + 2);
+            const float f = (row[0] == -INFINITY) ? 0.f : exp2f(row[0] - M);
+            L += row[1] * f;
+            O += row[2 + d] * f;
+        }
+        const float o = O / L;
+        const size_t orow = (size_t)s * p.num_q_heads + (size_t)h * g + n;
+        if (npart == 1) {
+            out[orow * D + d] = o;
+        } else {
+            const size_t r = orow * p.max_parts + part;
+            p.ws_o[r * D + d] = o;
+            if (d == 0) {
+                p.ws_ml[r * 2 + 0] = M;
+                p.ws_ml[r * 2 + 1] = L;
+            }
+        }
+    }
+}
+
+// =====================================================================================
+// K2: log-sum-exp merge of a sequence's partitions, one CTA of D threads per
+// (query head, sequence):  M = max_p m_p;  w_p = l_p 2^(m_p - M);
+//   out = sum_p w_p o_p / sum_p w_p.
+// Sequences with a single partition were written by K1 and are skipped.
+// =====================================================================================
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float *scratch) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = is_max ? fmaxf(v, w) : v + w;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    v = is_max ? -INFINITY : 0.f;
+    for (int w = 0; w < nw; ++w) v = is_max ? fmaxf(v, scratch[w]) : v + scratch[w];
+    return v;
+}
+
+template <typename OutT, int D>
+__global__ void __launch_bounds__(D) lse_reduce_kernel(const DecodeParams p) {
+    extern __shared__ float rsm[];  // [32] scratch + [max_parts] weights
+    const int hq = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
+    const int len = seq_len(p, s, false);
+    const int nblk = (len + kBlock - 1) / kBlock;
+    const int npart = (nblk + p.part_blocks - 1) / p.part_blocks;
+    if (npart <= 1) return;
+    const size_t row = (size_t)s * p.num_q_heads + hq;
+    const float *ml = p.ws_ml + row * p.max_parts * 2;
+    const float *o = p.ws_o + row * p.max_parts * D;
+    float *scratch = rsm;
+    float *w = rsm + 32;
+    float M = -INFINITY;
+    for (int i = tid; i < npart; i += D) M = fmaxf(M, ml[2 * i]);
+    M = block_reduce(M, true, scratch);
+    float W = 0.f;
+    for (int i = tid; i < npart; i += D) {
+        const float wi = ml[2 * i + 1] * exp2f(ml[2 * i] - M);
+        w[i] = wi;
+        W += wi;
+    }
+    W = block_reduce(W, false, scratch);
+    __syncthreads();
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int i = 0;
+    for (; i + 4 <= npart; i += 4) {
+        a0 = fmaf(w[i + 0], o[(size_t)(i + 0) * D + tid], a0);
+        a1 = fmaf(w[i + 1], o[(size_t)(i + 1) * D + tid], a1);
+        a2 = fmaf(w[i + 2], o[(size_t)(i + 2) * D + tid], a2);
+        a3 = fmaf(w[i + 3], o[(size_t)(i + 3) * D + tid], a3);
+    }
+    for (; i < npart; ++i) a0 = fmaf(w[i], o[(size_t)i * D + tid], a0);
+    const float r = ((a0 + a1) + (a2 + a3)) / W;
+    OutT *out = static_cast<OutT *>(p.out);
+    if constexpr (sizeof(OutT) == 2) {
+        out[row * D + tid] = __float2bfloat16_rn(r);
+    } else {
+        out[row * D + tid] = r;
+    }
+}
+
+// =====================================================================================
+// K3: KV append. One CTA per token; 16-byte vectors over (kv head, head-dim).
+// =====================================================================================
+__global__ void kv_append_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                 const int64_t *__restrict__ slots, uint4 *__restrict__ kc, uint4 *__restrict__ vc,
+                                 int num_kv_heads, int vec_per_row, int num_blocks) {
+    const int t = blockIdx.x;
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0) return;
+    if (slot >= (int64_t)num_blocks * kBlock) {
+        if (threadIdx.x == 0) raise_error(PKV_DEVERR_SLOT);
+        return;
+    }
+    const int64_t blk = slot >> 4;
+    const int off = (int)(slot & 15);
+    const int n = num_kv_heads * vec_per_row;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int hh = i / vec_per_row, c = i - hh * vec_per_row;
+        const size_t src = ((size_t)t * num_kv_heads + hh) * vec_per_row + c;
+        const size_t dst = (((size_t)blk * num_kv_heads + hh) * kBlock + off) * vec_per_row + c;
+        kc[dst] = __ldg(k + src);
+        vc[dst] = __ldg(v + src);
+    }
+}
+
+// =====================================================================================
+// K4: block copy. grid (chunks, pairs, 2 caches); 16-byte vectors.
+// =====================================================================================
+__global__ void copy_blocks_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc, const int64_t *__restrict__ pairs,
+                                   int num_blocks, int64_t vec_per_block) {
+    const int pr = blockIdx.y;
+    const int64_t src = __ldg(pairs + 2 * pr), dst = __ldg(pairs + 2 * pr + 1);
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0) raise_error(PKV_DEVERR_PAIR);
+        return;
+    }
+    uint4 *c = blockIdx.z ? vc : kc;
+    const uint4 *sp = c + src * vec_per_block;
+    uint4 *dp = c + dst * vec_per_block;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vec_per_block; i += (int64_t)gridDim.x * blockDim.x)
+        dp[i] = sp[i];
+}
+
+// =====================================================================================
+// K5: metadata checks (debug). They OR PKV_DEVERR_* bits into *err, never trap.
+// =====================================================================================
+__global__ void validate_tables_kernel(const int32_t *block_tables, const int32_t *context_lens, int max_blocks_per_seq,
+                                       int num_blocks, int max_context_len, int32_t *err) {
+    const int s = blockIdx.x;
+    int len = context_lens[s];
+    unsigned bits = 0;
+    if (len < 0 || len > max_blocks_per_seq * kBlock || len > max_context_len) bits |= PKV_DEVERR_LENGTH;
+    len = max(0, min(len, max_blocks_per_seq * kBlock));
+    const int nblk = (len + kBlock - 1) / kBlock;
+    for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
+        const int b = block_tables[(size_t)s * max_blocks_per_seq + j];
+        if (b < 0 || b >= num_blocks) bits |= PKV_DEVERR_BLOCK_ID;
+    }
+    if (bits) atomicOr(reinterpret_cast<unsigned *>(err), bits);
+}
+
+__global__ void validate_slots_kernel(const int64_t *slots, int num_tokens, int num_blocks, int32_t *err) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < num_tokens && slots[t] >= (int64_t)num_blocks * kBlock)
+        atomicOr(reinterpret_cast<unsigned *>(err), PKV_DEVERR_SLOT);
+}
+
+}  // namespace pkv

@@ -65,6 +65,8 @@ class WorkloadSpec:
     prompt_len: int = 0
     # extra copy pairs (tiny workload: two pairs into free blocks)
     extra_copy_pairs: int = 0
+    # lengths recipe "explicit": one context length per sequence
+    lengths_list: tuple = ()
 
 
 SPECS = {
@@ -87,7 +89,13 @@ CONFIG_ORDER = ["tiny", "mha13b", "gqa8b", "parallel_sampling", "long_context"]
 
 def spec(name: str, **overrides) -> WorkloadSpec:
     s = SPECS[name]
-    return dataclasses.replace(s, **overrides) if overrides else s
+    if "lengths_list" in overrides:
+        overrides.setdefault("lengths", "explicit")
+        overrides.setdefault("num_seqs", len(overrides["lengths_list"]))
+    s = dataclasses.replace(s, **overrides) if overrides else s
+    if s.lengths == "sampling" and s.num_seqs != s.num_prompts * s.samples_per_prompt:
+        s = dataclasses.replace(s, num_seqs=s.num_prompts * s.samples_per_prompt)
+    return s
 
 
 @dataclass
@@ -124,6 +132,10 @@ class Layout:
 
 
 def _lengths(sp: WorkloadSpec, rng: np.random.Generator) -> np.ndarray:
+    if sp.lengths == "explicit":
+        if len(sp.lengths_list) != sp.num_seqs:
+            raise ValueError("lengths_list must hold one length per sequence")
+        return np.array(sp.lengths_list, dtype=np.int64)
     if sp.lengths == "uniform":
         return rng.integers(sp.len_lo, sp.len_hi + 1, size=sp.num_seqs).astype(np.int64)
     if sp.lengths == "lognormal":

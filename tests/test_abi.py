@@ -1,0 +1,132 @@
+"""The C-ABI library loads, exports every function include/pagedkv.h
+declares, and rejects bad scalar arguments on the host -- all without a GPU
+(no call here reaches a kernel)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from paged_kv_cache_177_gb300.build import INCLUDE, build_library
+
+HEADER = os.path.join(INCLUDE, "pagedkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build_library()
+    return ctypes.CDLL(path)
+
+
+@pytest.fixture(scope="module")
+def binding(lib):
+    from paged_kv_cache_177_gb300 import binding as b
+    return b
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_three_calls_and_helpers():
+    names = declared_functions()
+    for required in ("paged_decode_attention", "kv_append", "copy_blocks", "pkv_status_string",
+                     "pkv_decode_workspace_bytes", "pkv_validate", "pkv_check_copy_pairs"):
+        assert required in names
+    assert len(names) >= 11
+
+
+def test_library_exports_every_declared_function(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_status_strings(binding):
+    assert binding.status_string(0) == "ok"
+    for code in (-1, -2, -3, -4, -5, -6, -7):
+        assert binding.status_string(code) not in ("ok", "unknown status")
+    assert binding.status_string(-99) == "unknown status"
+    assert binding.version() >= 100
+
+
+def test_partition_and_workspace_sizing(binding):
+    assert binding.partition_tokens(8, 8, 131072, 0) % 16 == 0
+    assert binding.partition_tokens(8, 8, 131072, 512) == 512
+    # a context no longer than one partition needs no workspace
+    assert binding.workspace_bytes(64, 40, 40, 128, 512, 512) == 0
+    # otherwise: S * Hq * ceil(L / P) * (2 + D) floats
+    assert binding.workspace_bytes(8, 64, 8, 128, 131072, 512) == 8 * 64 * 256 * 130 * 4
+    assert binding.workspace_bytes(2, 4, 4, 64, 1000, 64) == 2 * 4 * 16 * 66 * 4
+
+
+def _decode(lib, **kw):
+    args = dict(out=1 << 12, q=1 << 12, k=1 << 12, v=1 << 12, bt=1 << 12, cl=1 << 12, scale=0.1, hkv=8, S=4, hq=8,
+                d=64, maxb=4, nb=32, maxlen=64, dtype=0, pt=0, ws=None, wsb=0, stream=None)
+    args.update(kw)
+    f = lib.paged_decode_attention
+    f.restype = ctypes.c_int
+    vp = ctypes.c_void_p
+    f.argtypes = [vp] * 6 + [ctypes.c_float] + [ctypes.c_int] * 9 + [vp, ctypes.c_size_t, vp]
+    return f(args["out"], args["q"], args["k"], args["v"], args["bt"], args["cl"], args["scale"], args["hkv"],
+             args["S"], args["hq"], args["d"], args["maxb"], args["nb"], args["maxlen"], args["dtype"], args["pt"],
+             args["ws"], args["wsb"], args["stream"])
+
+
+def test_decode_rejects_bad_arguments_before_any_cuda_call(lib):
+    assert _decode(lib, d=96) == -2                  # unsupported head_dim
+    assert _decode(lib, dtype=7) == -2               # unsupported dtype
+    assert _decode(lib, hq=12, hkv=8) == -1          # heads not a multiple
+    assert _decode(lib, hq=8 * 17, hkv=8) == -2      # group of 17 > 16
+    assert _decode(lib, hkv=0) == -1
+    assert _decode(lib, S=-1) == -1
+    assert _decode(lib, out=None) == -1              # null pointer
+    assert _decode(lib, q=(1 << 12) + 4) == -7       # misaligned
+    assert _decode(lib, pt=24) == -1                 # partition not a multiple of 16
+    assert _decode(lib, maxlen=4096, pt=64) == -6    # split needed, no workspace
+    assert _decode(lib, scale=float("nan")) == -1
+    assert _decode(lib, S=0) == 0                    # empty batch: nothing to do
+
+
+def test_append_and_copy_reject_bad_arguments(lib):
+    vp, ci = ctypes.c_void_p, ctypes.c_int
+    ap = lib.kv_append
+    ap.restype = ci
+    ap.argtypes = [vp] * 5 + [ci] * 5 + [vp]
+    a = 1 << 12
+    assert ap(a, a, a, a, a, 4, 8, 96, 32, 0, None) == -2
+    assert ap(a, a, a, a, a, -1, 8, 64, 32, 0, None) == -1
+    assert ap(a, a + 8, a, a, a, 4, 8, 64, 32, 0, None) == -7
+    assert ap(a, a, a, a, a, 0, 8, 64, 32, 0, None) == 0
+    cp = lib.copy_blocks
+    cp.restype = ci
+    cp.argtypes = [vp] * 3 + [ci] * 5 + [vp]
+    assert cp(a, a, a, -1, 8, 64, 32, 0, None) == -1
+    assert cp(a, a, a, 2, 8, 64, 32, 3, None) == -2
+    assert cp(a, a, a, 0, 8, 64, 32, 0, None) == 0
+
+
+def test_host_pair_check(binding):
+    binding.check_copy_pairs(np.array([[0, 3], [1, 4]]), 8)
+    binding.check_copy_pairs(np.zeros((0, 2)), 8)
+    with pytest.raises(binding.PagedKVError) as e:
+        binding.check_copy_pairs(np.array([[0, 3], [1, 3]]), 8)     # repeated destination
+    assert e.value.code == -4
+    with pytest.raises(binding.PagedKVError) as e:
+        binding.check_copy_pairs(np.array([[0, 3], [3, 5]]), 8)     # destination also a source
+    assert e.value.code == -4
+    with pytest.raises(binding.PagedKVError) as e:
+        binding.check_copy_pairs(np.array([[0, 8]]), 8)
+    assert e.value.code == -3
+
+
+def test_binding_refuses_cpu_tensors(binding):
+    import torch
+    q = torch.zeros(1, 1, 64)
+    kc = torch.zeros(2, 1, 16, 64)
+    with pytest.raises(ValueError):
+        binding.paged_decode_attention(q.clone(), q, kc, kc, torch.zeros(1, 1, dtype=torch.int32),
+                                       torch.ones(1, dtype=torch.int32), 0.1, max_context_len=1)

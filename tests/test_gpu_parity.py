@@ -1,0 +1,243 @@
+"""GPU parity: the CUDA path (through the C-ABI binding) against the fp64
+oracle, element by element on the same seeded inputs.
+
+* KV append and block copy: bit-exact caches.
+* Attention: |gpu - ref| <= 2e-3 + 1e-2 |ref| for bf16, 1e-5 + 1e-5 |ref|
+  for fp32.
+Small cases span several blocks, several partitions and ragged tails; the
+full-size workloads run in the launch configuration the benchmark times and
+are checked on sampled sequences (all heads) plus size-independent
+properties on every output.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_177_gb300 import workloads as W
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+EDGE_LENGTHS = (0, 1, 15, 16, 17, 31, 33, 64, 100, 255, 511, 512, 513, 1000, 1537, 7)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(0)
+    b = H.lib()
+    b.device_error(clear=True)
+    yield
+    assert b.device_error(clear=True) == 0, "a kernel raised the device error word"
+
+
+def _parity(w_cpu, partition_tokens=0, seq_ids=None):
+    h = H.host_arrays(w_cpu)
+    w = w_cpu.to("cuda")
+    out = H.gpu_step(w, partition_tokens)
+    torch.cuda.synchronize()
+    ref = H.oracle_step(h, w.layout, w.scale, seq_ids)
+    H.assert_caches_equal(w, h)
+    got = out if seq_ids is None else out[torch.as_tensor(seq_ids, device=out.device)]
+    return H.assert_close(got, ref, w.spec.dtype, w.spec.name)
+
+
+def test_tiny_workload_full_step():
+    """fp32, 4 sequences, 8 heads, d=64, 32-block pool, 1-token append per
+    sequence and 2 copy pairs."""
+    _parity(W.make_workload("tiny"))
+
+
+CASES = [
+    # name, dtype, Hq, Hkv, d
+    ("mha_d128", "bf16", 4, 4, 128),
+    ("gqa4_d128", "bf16", 16, 4, 128),
+    ("gqa8_d128", "bf16", 16, 2, 128),
+    ("gqa16_d128", "bf16", 32, 2, 128),
+    ("gqa3_d64", "bf16", 6, 2, 64),
+    ("mha_d64", "bf16", 3, 3, 64),
+    ("gqa12_d64", "bf16", 12, 1, 64),
+    ("f32_gqa4_d128", "f32", 8, 2, 128),
+    ("f32_gqa16_d64", "f32", 16, 1, 64),
+]
+
+
+@pytest.mark.parametrize("partition_tokens", [0, 16, 48, 128])
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_small_cases_all_partitions(case, partition_tokens):
+    name, dt, hq, hkv, d = case
+    w = W.make_workload("gqa8b", lengths_list=EDGE_LENGTHS, num_q_heads=hq, num_kv_heads=hkv, head_dim=d, dtype=dt,
+                        seed=zlib.crc32(name.encode()) % 1000)
+    _parity(w, partition_tokens)
+
+
+def test_all_empty_and_single_sequence():
+    _parity(W.make_workload("gqa8b", lengths_list=(0, 0, 0)))
+    _parity(W.make_workload("gqa8b", lengths_list=(4096,)), partition_tokens=0)
+
+
+def test_outputs_are_bit_invariant_under_block_permutation():
+    """The same K/V placed on two different shuffles of the pool gives
+    bit-identical outputs (the kernel sees the same values in the same order)."""
+    b = H.lib()
+    w1 = W.make_workload("gqa8b", lengths_list=EDGE_LENGTHS, seed=7).to("cuda")
+    H.gpu_step(w1, attention=False)
+    perm = torch.randperm(w1.layout.num_blocks, generator=torch.Generator().manual_seed(3)).cuda()
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(perm.numel(), device=perm.device)
+    k2 = torch.empty_like(w1.k_cache)
+    v2 = torch.empty_like(w1.v_cache)
+    k2[perm] = w1.k_cache                      # block b moves to perm[b]
+    v2[perm] = w1.v_cache
+    t2 = perm[w1.block_tables.long()].int()
+    outs = []
+    for kc, vc, bt in ((w1.k_cache, w1.v_cache, w1.block_tables), (k2, v2, t2)):
+        out = torch.empty_like(w1.q)
+        b.paged_decode_attention(out, w1.q, kc, vc, bt, w1.context_lens, w1.scale,
+                                 max_context_len=w1.layout.max_context_len, partition_tokens=64)
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_shared_prefix_blocks_equal_duplicated_copies():
+    b = H.lib()
+    w = W.make_workload("parallel_sampling", num_prompts=3).to("cuda")
+    H.gpu_step(w, attention=False)
+    lay = w.layout
+    # duplicate every shared block into a fresh pool region and repoint the tables
+    bt = w.block_tables.long().clone()
+    S, maxb = bt.shape
+    nblk = (w.context_lens.long() + 15) // 16
+    mask = torch.arange(maxb, device=bt.device)[None, :] < nblk[:, None]
+    n_entries = int(mask.sum())
+    k2 = torch.cat([w.k_cache, w.k_cache[bt[mask]]])
+    v2 = torch.cat([w.v_cache, w.v_cache[bt[mask]]])
+    t2 = bt.clone()
+    t2[mask] = lay.num_blocks + torch.arange(n_entries, device=bt.device)
+    outs = []
+    for kc, vc, tb in ((w.k_cache, w.v_cache, w.block_tables), (k2, v2, t2.int())):
+        out = torch.empty_like(w.q)
+        b.paged_decode_attention(out, w.q, kc, vc, tb, w.context_lens, w.scale, max_context_len=lay.max_context_len)
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_step_on_a_side_stream_and_in_a_cuda_graph():
+    """The three calls are stream-ordered on the caller's stream and capture
+    into a CUDA graph (no host synchronisation, caller-owned workspace)."""
+    b = H.lib()
+    wc = W.make_workload("parallel_sampling", num_prompts=2)
+    h = H.host_arrays(wc)
+    ref = H.oracle_step(h, wc.layout, wc.scale)
+    w = wc.to("cuda")
+    lay = w.layout
+    ws = torch.empty(max(1, b.workspace_bytes(lay.spec.num_seqs, lay.spec.num_q_heads, lay.spec.num_kv_heads,
+                                                lay.spec.head_dim, lay.max_context_len, 64)),
+                     dtype=torch.uint8, device="cuda")
+    k0, v0 = w.k_cache.clone(), w.v_cache.clone()
+    out = torch.empty_like(w.q)
+    s = torch.cuda.Stream()
+
+    def step():
+        b.copy_blocks(w.k_cache, w.v_cache, w.cow_pairs, check=False, stream=s)
+        b.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache, stream=s)
+        b.paged_decode_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
+                                 max_context_len=lay.max_context_len, partition_tokens=64, workspace=ws, stream=s)
+
+    b.check_copy_pairs(lay.cow_pairs, lay.num_blocks)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    s.synchronize()
+    H.assert_close(out, ref, "bf16", "side stream")
+    H.assert_caches_equal(w, h)
+    # graph: restore the pre-step caches, capture, replay twice
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for _ in range(2):
+        w.k_cache.copy_(k0)
+        w.v_cache.copy_(v0)
+        out.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        H.assert_close(out, ref, "bf16", "graph replay")
+        H.assert_caches_equal(w, h)
+
+
+def test_device_error_word_and_validators():
+    """Bad device contents never fault: the kernels skip or zero-fill the bad
+    element and raise a bit in the device error word; the validators flag
+    the metadata without running the step."""
+    b = H.lib()
+    w = W.make_workload("gqa8b", lengths_list=(40, 3, 70)).to("cuda")
+    lay = w.layout
+    b.device_error(clear=True)
+    err = b.validate(w.block_tables, w.context_lens, lay.num_blocks, lay.max_context_len)
+    assert int(err.item()) == 0
+    bad_tables = w.block_tables.clone()
+    bad_tables[0, 1] = lay.num_blocks + 5
+    err = b.validate(bad_tables, w.context_lens, lay.num_blocks, lay.max_context_len)
+    assert int(err.item()) == b.DEVERR_BLOCK_ID
+    too_long = w.context_lens.clone()
+    too_long[1] = lay.max_context_len + 1
+    err = b.validate(w.block_tables, too_long, lay.num_blocks, lay.max_context_len)
+    assert int(err.item()) == b.DEVERR_LENGTH
+    bad_slots = w.slot_mapping.clone()
+    bad_slots[0] = lay.num_blocks * 16
+    assert int(b.validate_slots(bad_slots, lay.num_blocks).item()) == b.DEVERR_SLOT
+    assert int(b.validate_slots(w.slot_mapping, lay.num_blocks).item()) == 0
+    assert b.device_error(clear=True) == 0
+
+    out = torch.empty_like(w.q)
+    b.paged_decode_attention(out, w.q, w.k_cache, w.v_cache, bad_tables, w.context_lens, w.scale,
+                             max_context_len=lay.max_context_len)
+    torch.cuda.synchronize()
+    assert b.device_error(clear=True) == b.DEVERR_BLOCK_ID
+    b.kv_append(w.k_new, w.v_new, bad_slots, w.k_cache, w.v_cache)
+    torch.cuda.synchronize()
+    assert b.device_error(clear=True) == b.DEVERR_SLOT
+    bad_pairs = torch.tensor([[0, lay.num_blocks]], dtype=torch.int64, device="cuda")
+    b.copy_blocks(w.k_cache, w.v_cache, bad_pairs, check=False)
+    torch.cuda.synchronize()
+    assert b.device_error(clear=True) == b.DEVERR_PAIR
+    with pytest.raises(b.PagedKVError):
+        b.copy_blocks(w.k_cache, w.v_cache, bad_pairs)            # host check rejects it
+    b.paged_decode_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, too_long, w.scale,
+                             max_context_len=lay.max_context_len)
+    torch.cuda.synchronize()
+    assert b.device_error(clear=True) == b.DEVERR_LENGTH
+
+
+# ---- full-size workloads, in the benchmark's launch configuration ----------------------
+
+FULL = {
+    # name: sampled sequences checked against the oracle (all heads)
+    "mha13b": 8,
+    "gqa8b": 8,
+    "parallel_sampling": 8,
+    "long_context": 2,
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_workload(name):
+    w = W.make_workload(name, device="cuda")
+    lay = w.layout
+    h = H.host_arrays(w)
+    out = H.gpu_step(w, lay.spec.partition_tokens)
+    torch.cuda.synchronize()
+    order = np.argsort(lay.context_lens, kind="stable")
+    extra = np.random.default_rng(0).choice(len(order), max(0, FULL[name] - 2), replace=False).tolist()
+    pick = sorted(set([int(order[-1]), int(order[0])] + extra))
+    ref = H.oracle_step(h, lay, w.scale, seq_ids=pick)
+    H.assert_caches_equal(w, h)
+    H.assert_close(out[torch.as_tensor(pick, device="cuda")], ref, lay.spec.dtype, name)
+    # every output: finite, and a convex combination of values that are N(0,1)-sized
+    o = out.float()
+    assert torch.isfinite(o).all()
+    vmax = torch.nan_to_num(w.v_cache.float(), nan=0.0).abs().max()
+    assert float(o.abs().max()) <= float(vmax) * (1 + 1e-2)
