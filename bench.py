@@ -180,9 +180,11 @@ def cpu_cores() -> int:
 
 def oracle_sample(lay: W.Layout, host: dict, target_s: float):
     """Times the oracle (fp64, all host cores) on a bounded sample of the
-    workload's sequences -- about ``target_s`` seconds of CPU work -- after
-    applying the step's copies and appends on the host.  Returns
-    (GB/s, seconds, sequences, sample bytes)."""
+    workload -- about ``target_s`` seconds of CPU work -- after applying the
+    step's copies and appends on the host.  The sample grows by sequences
+    until one pass takes a quarter of the budget (or covers the workload),
+    then passes repeat until the budget is spent.  Returns
+    (GB/s, seconds, sequences, passes, sample bytes per pass)."""
     import oracle
 
     eb = 2 if lay.spec.dtype == "bf16" else 4
@@ -201,11 +203,15 @@ def oracle_sample(lay: W.Layout, host: dict, target_s: float):
     n = min(len(order), max(1, cpu_cores() // max(1, lay.spec.num_kv_heads)))
     dt = run(order[:n])
     while dt < target_s / 4 and n < len(order):
-        n = min(len(order), int(n * max(2.0, target_s / max(dt, 1e-3) * 0.5)))
+        n = min(len(order), max(n + 1, int(n * min(8.0, target_s / 4 / max(dt, 1e-4)))))
         dt = run(order[:n])
     ids = order[:n]
+    total, passes = dt, 1
+    while total < target_s:
+        total += run(ids)
+        passes += 1
     nbytes = int(lay.context_lens[ids].astype(np.int64).sum()) * per_token
-    return nbytes / dt / 1e9, dt, int(n), nbytes
+    return nbytes * passes / total / 1e9, total, int(n), passes, nbytes
 
 
 def run_reference(args, rank, world, dist):
@@ -279,48 +285,79 @@ def run_ours(args, rank, world, local, dist):
     split = B.partition_tokens(S, Hkv, maxlen, pt) < maxlen
     launches_per_step = (1 if has_pairs else 0) + 1 + 1 + (1 if split else 0)
     B.check_copy_pairs(lay.cow_pairs, lay.num_blocks)
-    # the step rewrites the same slots and blocks every time, so repeating it is idempotent
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    # per-step inputs live in buffers of their own, so the end-to-end run can
+    # refill them from pinned host memory; the step rewrites the same slots and
+    # blocks every time, so repeating it is idempotent
+    host_in = [t.to("cpu").pin_memory() for t in (w.q, w.k_new, w.v_new, w.slot_mapping, w.block_tables,
+                                                 w.context_lens, w.cow_pairs)]
+    dev_in = [t.to(dev) for t in host_in]
+    q, k_new, v_new, slots, tables, lens, pairs = dev_in
+    evict = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev).fill_(1.0)
 
-    def step(q, k_new, v_new, slots, tables, lens, pairs, attn_events=None):
+    def flush_l2():
+        evict.sum()           # reads 256 MiB: evicts K/V lines without leaving dirty ones
+
+    def pre():
         if has_pairs:
             B.copy_blocks(w.k_cache, w.v_cache, pairs, check=False, stream=stream)
         B.kv_append(k_new, v_new, slots, w.k_cache, w.v_cache, stream=stream)
-        if attn_events is not None:
-            attn_events[0].record(stream)
+
+    def attn():
         B.paged_decode_attention(out, q, w.k_cache, w.v_cache, tables, lens, w.scale, max_context_len=maxlen,
                                  partition_tokens=pt, workspace=ws, stream=stream)
-        if attn_events is not None:
-            attn_events[1].record(stream)
 
-    dev_inputs = (w.q, w.k_new, w.v_new, w.slot_mapping, w.block_tables, w.context_lens, w.cow_pairs)
     stream.wait_stream(torch.cuda.current_stream(dev))
-    torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            flush.fill_(1.0)
-            step(*dev_inputs)
+            flush_l2()
+            pre()
+            attn()
     torch.cuda.synchronize(dev)
     if B.device_error(clear=True):
         raise RuntimeError("device error word set during warm-up")
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    aev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # the step as a CUDA graph: a decode loop replays it without host launch work;
+    # the attention call alone is a second graph, timed separately for the roofline
+    g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream):
+        pre()
+        attn()
+    with torch.cuda.graph(g_attn, stream=stream):
+        attn()
+    torch.cuda.synchronize(dev)
+
+    steps = args.steps
+    if steps is None:
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(20):
+                flush_l2()
+                g_step.replay()
+        torch.cuda.synchronize(dev)
+        steps = int(min(20000, max(200, 1.5 / ((time.perf_counter() - t0) / 20))))
+
+    def timed(graph, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                flush_l2()                 # untimed
+                evs[i][0].record(stream)
+                graph.replay()
+                evs[i][1].record(stream)
+        return evs
+
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
         wall0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                flush.fill_(1.0)          # evict the previous step's lines from L2 (not timed)
-                ev[i][0].record(stream)
-                step(*dev_inputs, attn_events=aev[i])
-                ev[i][1].record(stream)
+        ev = timed(g_step, steps)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
     if dist is not None:
         dist.barrier()
+    aev = timed(g_attn, min(steps, 2000))
+    torch.cuda.synchronize(dev)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     attn_ms = [a.elapsed_time(b) for a, b in aev]
     t_step = sum(step_ms) / len(step_ms) / 1e3
@@ -329,26 +366,26 @@ def run_ours(args, rank, world, local, dist):
     total_bytes = sum_over_ranks(nbytes["total"], dist, dev)
     value = total_bytes / t_step_max / 1e9
 
-    # ---- end to end through the C ABI: per-step inputs in pinned host memory ----
-    host_in = [t.to("cpu").pin_memory() for t in dev_inputs]
-    dev_in = [torch.empty_like(t) for t in dev_inputs]
+    # ---- end to end: per-step inputs copied in from pinned host memory and the
+    # output copied back, inside the timed region ----
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = host_out.numel() * host_out.element_size()
-    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e2e_steps = min(steps, 2000)
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
     with torch.cuda.stream(stream):
-        for i in range(args.warmup + args.steps):
-            flush.fill_(1.0)
+        for i in range(args.warmup + e2e_steps):
+            flush_l2()
             if i >= args.warmup:
                 eev[i - args.warmup][0].record(stream)
             for dst, src in zip(dev_in, host_in):
                 dst.copy_(src, non_blocking=True)
-            step(*dev_in)
+            g_step.replay()
             host_out.copy_(out, non_blocking=True)
             if i >= args.warmup:
                 eev[i - args.warmup][1].record(stream)
     torch.cuda.synchronize(dev)
-    t_e2e = sum(a.elapsed_time(b) for a, b in eev) / args.steps / 1e3
+    t_e2e = sum(a.elapsed_time(b) for a, b in eev) / e2e_steps / 1e3
     t_e2e_max = max_over_ranks(t_e2e, dist, dev)
     e2e_value = total_bytes / t_e2e_max / 1e9
     err = B.device_error(clear=True)
@@ -364,16 +401,17 @@ def run_ours(args, rank, world, local, dist):
         # the device caches already hold the step's copies and appends; the oracle
         # re-applies them on the host (idempotent) before attending
         host = {k: W.to_numpy(getattr(w, k)) for k in ("q", "k_cache", "v_cache", "k_new", "v_new")}
-        gbs, secs, nseq, sb = oracle_sample(lay, host, args.cpu_seconds)
+        gbs, secs, nseq, passes, sb = oracle_sample(lay, host, args.cpu_seconds)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"{nseq} of {S} sequences ({sb / 1e6:.1f} MB of K/V, all heads) in {secs:.1f} s, fp64 C "
-                         "oracle, after the step's copies and appends"}
+               "sample": f"{nseq} of {S} sequences ({sb / 1e6:.1f} MB of K/V, all heads) x {passes} passes in "
+                         f"{secs:.1f} s, fp64 C oracle, after the step's copies and appends"}
+    srt = sorted(step_ms)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": world,
-        "steps": args.steps,
+        "steps": steps,
         "warmup": args.warmup,
         "ms_per_step": round(t_step_max * 1e3, 4),
         "higher_is_better": True,
@@ -384,27 +422,29 @@ def run_ours(args, rank, world, local, dist):
         "config": {
             "workload": describe(sp),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "step": ("copy_blocks + " if has_pairs else "") + "kv_append + paged_decode_attention",
+            "step": ("copy_blocks + " if has_pairs else "") + "kv_append + paged_decode_attention, "
+                    "replayed as one CUDA graph",
             "partition_tokens": B.partition_tokens(S, Hkv, maxlen, pt),
             "max_context_len": maxlen,
             "tokens": int(lay.context_lens.sum()),
             "step_bytes": nbytes,
-            "l2": "flushed between steps (256 MiB write, untimed) and K/V larger than L2",
+            "l2": "evicted between steps by reading a 256 MiB buffer (untimed); K/V larger than L2",
         },
         "us_per_step": round(t_step_max * 1e6, 2),
+        "us_per_step_p10_p90": [round(srt[len(srt) // 10] * 1e3, 2), round(srt[(9 * len(srt)) // 10] * 1e3, 2)],
         "seqs_per_s": round(S * world / t_step_max, 1),
         "pct_hbm_peak": {"measured": round(100 * value / world / peak, 2),
                          "nominal_7.9TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2)},
         "roofline": {
             "kernel": "paged_decode_attention (decode_bf16_kernel" + (" + lse_reduce_kernel)" if split else ")"),
             "bound": "hbm", "achieved": round(attn_gbs, 2), "peak": peak, "unit": "GB/s",
-            "frac": round(attn_gbs / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
-            "traffic": None, "us_per_launch": round(t_attn * 1e6, 2),
+            "frac": round(attn_gbs / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+            "traffic": None, "us_per_launch": round(t_attn * 1e6, 2), "timed_launches": len(attn_ms),
             "bytes_per_launch": nbytes["attention"],
         },
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(t_e2e_max * 1e3, 4)},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step * steps,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
         "wall_s_timed_region": round(wall, 3),
@@ -415,17 +455,20 @@ def run_ours(args, rank, world, local, dist):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for about 1.5 s of device time)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mha13b", choices=list(W.SPECS))
     ap.add_argument("--partition-tokens", type=int, default=None)
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.impl == "reference" and args.steps is None:
+        args.steps = 5
     rank, world, local, dist = dist_setup(args)
     if args.gpus != world and world > 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
