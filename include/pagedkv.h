@@ -168,6 +168,44 @@ int pkv_validate_slots(const int64_t *slot_mapping, int num_tokens, int num_bloc
  */
 int pkv_device_error(uint32_t *value, int clear);
 
+/*
+ * Bytes of the library's built-in decode scratch (32 MiB), used by
+ * paged_decode_attention_static_workspace.
+ */
+#define PKV_STATIC_WORKSPACE_BYTES (32u << 20)
+
+/*
+ * paged_decode_attention without a caller-provided workspace. No part of the
+ * pages corresponds to this call: it exists for callers that cannot allocate
+ * device memory where they call the library -- e.g. a plugin or extension hook
+ * that is handed raw device pointers and has no allocator of its own, or a
+ * serving loop that owns every byte of device memory from start-up and forbids
+ * later cudaMalloc (which can synchronise the device, fail under a fixed
+ * budget, or fragment a carefully sized pool).
+ *
+ * Arguments, layout, results and errors are those of paged_decode_attention;
+ * the split-context scratch lives instead in a file-scope device array of
+ * PKV_STATIC_WORKSPACE_BYTES that every GPU which loads the library holds
+ * until the process exits. A call whose split needs more than that returns
+ * PKV_ERR_WORKSPACE and launches nothing (a larger partition_tokens needs
+ * less scratch). The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current and caches it; make that first call before any stream
+ * capture. All calls share the one array and it keeps the last call's
+ * contents; nothing in it needs to start at zero, because every partial
+ * result a call reads was written earlier by the same call. Calls that
+ * overlap on the GPU (different streams, or different host threads, without
+ * ordering between them) race on the array: order them, or use
+ * paged_decode_attention with separate workspaces.
+ */
+int paged_decode_attention_static_workspace(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                            const int32_t *block_tables, const int32_t *context_lens, float scale,
+                                            int num_kv_heads, int num_seqs, int num_q_heads, int head_dim,
+                                            int max_blocks_per_seq, int num_blocks, int max_context_len,
+                                            pkv_dtype dtype, int partition_tokens, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -296,3 +296,106 @@ int pkv_device_error(uint32_t *value, int clear) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode without a caller-provided workspace (see pagedkv.h): the scratch is a
+// file-scope device array whose device address is looked up once per device.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_static_workspace[PKV_STATIC_WORKSPACE_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_workspace_mu;
+void *g_static_workspace_ptr[kMaxDevices] = {};
+
+// Device address of g_static_workspace on the current device. In host code the
+// array's name is only a host-side stand-in, so it is resolved with
+// cudaGetSymbolAddress, with that device current, the first time.
+int static_workspace_address(void **ptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_static_workspace_mu);
+    if (!g_static_workspace_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return PKV_ERR_CUDA;
+        g_static_workspace_ptr[dev] = p;
+    }
+    *ptr = g_static_workspace_ptr[dev];
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int paged_decode_attention_static_workspace(void *out, const void *q, const void *k_cache,
+                                                       const void *v_cache, const int32_t *block_tables,
+                                                       const int32_t *context_lens, float scale, int num_kv_heads,
+                                                       int num_seqs, int num_q_heads, int head_dim,
+                                                       int max_blocks_per_seq, int num_blocks, int max_context_len,
+                                                       pkv_dtype dtype, int partition_tokens, void *stream) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+        max_context_len < 0 || partition_tokens < 0)
+        return PKV_ERR_ARG;
+    if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0) return PKV_ERR_ARG;
+    const int g = num_q_heads / num_kv_heads;
+    if (g > 16) return PKV_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return PKV_ERR_ARG;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)num_blocks * num_kv_heads * 16 >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+    const int pt = pkv_decode_partition_tokens(num_seqs, num_kv_heads, max_context_len, partition_tokens);
+    if (pt % 16 != 0) return PKV_ERR_ARG;
+    const int mp = max_parts_for(max_context_len, pt);
+    if (mp > kMaxParts) return PKV_ERR_UNSUPPORTED;
+    const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                                                   partition_tokens);
+    if (need > PKV_STATIC_WORKSPACE_BYTES) return PKV_ERR_WORKSPACE;
+    void *workspace = nullptr;
+    if (need > 0) {
+        const int rc = static_workspace_address(&workspace);
+        if (rc != PKV_OK) return rc;
+    }
+
+    pkv::DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.ws_ml = static_cast<float *>(workspace);
+    p.ws_o = need ? static_cast<float *>(workspace) + (size_t)num_seqs * num_q_heads * mp * 2 : nullptr;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = g;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.max_context_len = max_context_len;
+    p.part_blocks = pt / 16;
+    p.max_parts = mp;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    dim3 grid(mp, num_kv_heads, num_seqs);
+    int rc;
+    if (dtype == PKV_BF16) {
+        alignas(64) CUtensorMap tmk, tmv;
+        if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
+        if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
+        if (head_dim == 128)
+            rc = g <= 8 ? launch_bf16<128, 1>(tmk, tmv, p, grid, st) : launch_bf16<128, 2>(tmk, tmv, p, grid, st);
+        else
+            rc = g <= 8 ? launch_bf16<64, 1>(tmk, tmv, p, grid, st) : launch_bf16<64, 2>(tmk, tmv, p, grid, st);
+    } else {
+        rc = head_dim == 128 ? launch_f32<128>(p, grid, st) : launch_f32<64>(p, grid, st);
+    }
+    if (rc != PKV_OK) return rc;
+    if (mp > 1) rc = head_dim == 128 ? launch_reduce<128>(p, dtype, st) : launch_reduce<64>(p, dtype, st);
+    return rc;
+}
