@@ -278,12 +278,13 @@ def run_ours(args, rank, world, local, dist):
     maxlen = lay.max_context_len
     nbytes = step_bytes(lay)
     ws_bytes = B.workspace_bytes(S, Hq, Hkv, D, maxlen, pt)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)   # zero-filled once, as required
     out = torch.empty_like(w.q)
     stream = torch.cuda.Stream(dev)
     has_pairs = len(lay.cow_pairs) > 0
-    split = B.partition_tokens(S, Hkv, maxlen, pt) < maxlen
-    launches_per_step = (1 if has_pairs else 0) + 1 + 1 + (1 if split else 0)
+    attn_launches = B.decode_launches(S, Hkv, maxlen, pt, w.q.dtype)
+    persistent = pt <= 0 and sp.dtype == "bf16" and attn_launches == 1 and maxlen > B.partition_tokens(S, Hkv, maxlen, pt)
+    launches_per_step = (1 if has_pairs else 0) + 1 + attn_launches
     B.check_copy_pairs(lay.cow_pairs, lay.num_blocks)
     # per-step inputs live in buffers of their own, so the end-to-end run can
     # refill them from pinned host memory; the step rewrites the same slots and
@@ -316,13 +317,10 @@ def run_ours(args, rank, world, local, dist):
     if B.device_error(clear=True):
         raise RuntimeError("device error word set during warm-up")
 
-    # the step as a CUDA graph: a decode loop replays it without host launch work;
-    # the attention call alone is a second graph, timed separately for the roofline
-    g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    # the step as a CUDA graph: a decode loop replays it without host launch work
+    g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step, stream=stream):
         pre()
-        attn()
-    with torch.cuda.graph(g_attn, stream=stream):
         attn()
     torch.cuda.synchronize(dev)
 
@@ -356,7 +354,19 @@ def run_ours(args, rank, world, local, dist):
         wall = time.perf_counter() - wall0
     if dist is not None:
         dist.barrier()
-    aev = timed(g_attn, min(steps, 2000))
+    # the attention call alone, launched straight through the C ABI with its
+    # arguments marshalled once (the eviction read in front of each call keeps
+    # the GPU busy while the host enqueues, so host time is not in the window)
+    attn_args = B.decode_args(out, q, w.k_cache, w.v_cache, tables, lens, w.scale, max_context_len=maxlen,
+                              partition_tokens=pt, workspace=ws, stream=stream)
+    n_attn = min(steps, 2000)
+    aev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_attn)]
+    with torch.cuda.stream(stream):
+        for i in range(n_attn):
+            flush_l2()
+            aev[i][0].record(stream)
+            B.decode_raw(attn_args)
+            aev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     attn_ms = [a.elapsed_time(b) for a, b in aev]
@@ -424,7 +434,7 @@ def run_ours(args, rank, world, local, dist):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "step": ("copy_blocks + " if has_pairs else "") + "kv_append + paged_decode_attention, "
                     "replayed as one CUDA graph",
-            "partition_tokens": B.partition_tokens(S, Hkv, maxlen, pt),
+            "partition_tokens": "balanced (persistent kernel)" if persistent else B.partition_tokens(S, Hkv, maxlen, pt),
             "max_context_len": maxlen,
             "tokens": int(lay.context_lens.sum()),
             "step_bytes": nbytes,
@@ -436,7 +446,8 @@ def run_ours(args, rank, world, local, dist):
         "pct_hbm_peak": {"measured": round(100 * value / world / peak, 2),
                          "nominal_7.9TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2)},
         "roofline": {
-            "kernel": "paged_decode_attention (decode_bf16_kernel" + (" + lse_reduce_kernel)" if split else ")"),
+            "kernel": "paged_decode_attention (" + ("decode_bf16_persistent_kernel" if persistent else
+                                                    "decode_bf16_kernel" + (" + lse_reduce_kernel" if attn_launches == 2 else "")) + ")",
             "bound": "hbm", "achieved": round(attn_gbs, 2), "peak": peak, "unit": "GB/s",
             "frac": round(attn_gbs / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
             "traffic": None, "us_per_launch": round(t_attn * 1e6, 2), "timed_launches": len(attn_ms),

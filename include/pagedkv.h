@@ -67,6 +67,9 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_ERR_WORKSPACE -6    /* workspace missing or smaller than pkv_decode_workspace_bytes */
 #define PKV_ERR_ALIGN -7        /* a pointer is not 16-byte aligned */
 
+/* partition_tokens value that asks for the persistent balanced split (bf16). */
+#define PKV_PARTITION_BALANCED -1
+
 /* Bits of the device error word. */
 #define PKV_DEVERR_BLOCK_ID 0x1u    /* a block-table entry outside [0, num_blocks): its K/V read as zeros */
 #define PKV_DEVERR_SLOT 0x2u        /* a slot >= num_blocks*16 in kv_append: that token was skipped */
@@ -81,19 +84,39 @@ const char *pkv_status_string(int status);
 int pkv_version(void);
 
 /*
- * Effective tokens per split-context partition for a decode call (a multiple
- * of 16). partition_tokens > 0 is returned as is (it must be a multiple of
- * 16); 0 asks for the library's choice. A sequence of L tokens is processed
- * as ceil(L / partition) partitions whose partial softmax statistics are
- * merged by a log-sum-exp reduce; the result does not depend on the choice.
+ * Tokens per split-context partition for a decode call (a multiple of 16):
+ * partition_tokens > 0 is returned as is (it must be a multiple of 16); 0
+ * (automatic) and PKV_PARTITION_BALANCED give 512. A sequence of L tokens is
+ * processed as ceil(L / partition) partitions whose partial softmax
+ * statistics are merged by a log-sum-exp reduce; the result does not depend
+ * on the choice.
+ *
+ * bf16 has a second decomposition, chosen with PKV_PARTITION_BALANCED, or
+ * automatically (partition_tokens == 0) when the batch has at least a quarter
+ * as many (sequence, kv head) pairs as the GPU runs persistent warps (16 per
+ * SM): the blocks of all pairs are cut into equal shares, one per warp of a
+ * persistent kernel (one CTA per SM), and the pieces of a cut sequence are
+ * merged with the same log-sum-exp rule inside that kernel. Batches of a few
+ * long sequences keep fixed partitions, which merge faster.
  */
 int pkv_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_len, int partition_tokens);
 
 /*
+ * Kernel launches one paged_decode_attention call makes with these arguments:
+ * 1 (persistent balanced kernel, or no sequence longer than one partition),
+ * 2 (partition kernel + log-sum-exp reduce kernel), 0 for an empty batch or
+ * bad arguments. Queries the current device's SM count.
+ */
+int pkv_decode_launches(int num_seqs, int num_kv_heads, int max_context_len, int partition_tokens, pkv_dtype dtype);
+
+/*
  * Bytes of device workspace paged_decode_attention needs with these
- * arguments (0 when no sequence can span more than one partition). The
- * workspace holds, per (sequence, query head, partition), the running max and
- * sum of the softmax (log2 domain) and the partial output, all fp32.
+ * arguments (0 when it needs none). The workspace holds per-sequence arrival
+ * counters and partial softmax states (max in the log2 domain, sum, partial
+ * output, fp32). It must be zero-filled before the first call that uses it
+ * (for example cudaMemsetAsync once after allocating it); every call that
+ * completes without a device error leaves it zero-filled again, so it can be
+ * reused call after call without clearing.
  */
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                   int max_context_len, int partition_tokens);
@@ -110,8 +133,9 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
  *   launch); longer lengths are clamped and flagged (PKV_DEVERR_LENGTH).
  * A context length of 0 yields a zero output row.
  * workspace / workspace_bytes: device scratch of at least
- *   pkv_decode_workspace_bytes(...) bytes (may be NULL when that is 0).
- *   Concurrent calls must not share a workspace.
+ *   pkv_decode_workspace_bytes(...) bytes, zero-filled before its first use
+ *   (may be NULL when that size is 0). Concurrent calls must not share a
+ *   workspace. After a call that raised PKV_DEVERR_TIMEOUT, zero it again.
  */
 int paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                            const int32_t *block_tables, const int32_t *context_lens, float scale,
@@ -194,8 +218,10 @@ int pkv_device_error(uint32_t *value, int clear);
  * The first call on a device looks up the array's device address with that
  * device current and caches it; make that first call before any stream
  * capture. All calls share the one array and it keeps the last call's
- * contents; nothing in it needs to start at zero, because every partial
- * result a call reads was written earlier by the same call. Calls that
+ * contents; nothing else in it needs to start at zero, because every partial
+ * result a call reads was written earlier by the same call, and the arrival
+ * counters it uses start at zero when the library loads and are left at zero
+ * by every call that completes without a device error. Calls that
  * overlap on the GPU (different streams, or different host threads, without
  * ordering between them) race on the array: order them, or use
  * paged_decode_attention with separate workspaces.

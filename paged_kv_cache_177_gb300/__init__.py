@@ -14,7 +14,7 @@ __version__ = "0.1.0"
 
 _BINDING_NAMES = {
     "paged_decode_attention", "kv_append", "copy_blocks", "check_copy_pairs", "validate", "validate_slots",
-    "device_error", "workspace_bytes", "partition_tokens", "status_string", "version", "PagedKVError",
+    "device_error", "workspace_bytes", "partition_tokens", "decode_launches", "status_string", "version", "PagedKVError",
 }
 
 

@@ -24,6 +24,7 @@ if not os.path.exists(LIB):
 _lib = ctypes.CDLL(LIB)
 
 PKV_F32, PKV_BF16 = 0, 1
+PARTITION_AUTO, PARTITION_BALANCED = 0, -1
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_PAIR, DEVERR_TIMEOUT, DEVERR_LENGTH = 0x1, 0x2, 0x4, 0x8, 0x10
 BLOCK_SIZE = 16
 
@@ -41,6 +42,7 @@ _status_string = _decl("pkv_status_string", ctypes.c_char_p, _i)
 _version = _decl("pkv_version", _i)
 _partition_tokens = _decl("pkv_decode_partition_tokens", _i, _i, _i, _i, _i)
 _workspace_bytes = _decl("pkv_decode_workspace_bytes", _sz, _i, _i, _i, _i, _i, _i)
+_decode_launches = _decl("pkv_decode_launches", _i, _i, _i, _i, _i, _i)
 _decode = _decl("paged_decode_attention", _i, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                 _vp, _sz, _vp)
 _append = _decl("kv_append", _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
@@ -108,18 +110,21 @@ def workspace_bytes(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim
     return int(_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, partition_tokens))
 
 
-def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
-                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
-                           num_kv_heads: Optional[int] = None, *, max_context_len: Optional[int] = None,
-                           partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
-                           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """out[s, hq] = softmax(scale * K_s q[s, hq]) V_s over context_lens[s] tokens
-    read through block_tables[s]; see include/pagedkv.h.
+def decode_launches(num_seqs: int, num_kv_heads: int, max_context_len: int, partition_tokens: int = 0,
+                    dtype: torch.dtype = torch.bfloat16) -> int:
+    """Kernel launches of one decode call: 1 (persistent balanced kernel, or
+    no split), 2 (partition kernel + reduce), 0 (empty batch)."""
+    code = PKV_BF16 if dtype == torch.bfloat16 else PKV_F32
+    return int(_decode_launches(num_seqs, num_kv_heads, max_context_len, partition_tokens, code))
 
-    q, out: [S, Hq, D]; k_cache, v_cache: [NB, Hkv, 16, D] (bf16 or fp32,
-    all one dtype); block_tables int32 [S, maxB]; context_lens int32 [S].
-    ``max_context_len`` defaults to context_lens.max() (a device sync).
-    """
+
+def decode_args(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                num_kv_heads: Optional[int] = None, *, max_context_len: Optional[int] = None,
+                partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> tuple:
+    """Checks and marshals the arguments of one paged_decode_attention call
+    (see there) into the C-ABI argument tuple, for ``decode_raw``."""
     dev = _dev(out, q, k_cache, v_cache, block_tables, context_lens)
     dt = _dtype_code(q)
     if not (out.dtype == q.dtype == k_cache.dtype == v_cache.dtype):
@@ -138,14 +143,40 @@ def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
         max_context_len = int(context_lens.max().item()) if S else 0
     need = workspace_bytes(S, Hq, Hkv, D, max_context_len, partition_tokens)
     if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)   # must start zero-filled
     if workspace is not None:
         _dev(workspace)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = _decode(_p(out), _p(q), _p(k_cache), _p(v_cache), _p(block_tables), _p(context_lens), float(scale), Hkv, S,
-                 Hq, D, block_tables.shape[1], NB, int(max_context_len), dt, int(partition_tokens), _p(workspace),
-                 ws_bytes, _stream_ptr(dev, stream))
-    _check(rc, "paged_decode_attention")
+    # the tensors ride along so they outlive the raw pointers
+    return ((_p(out), _p(q), _p(k_cache), _p(v_cache), _p(block_tables), _p(context_lens), float(scale), Hkv, S, Hq,
+             D, block_tables.shape[1], NB, int(max_context_len), dt, int(partition_tokens), _p(workspace), ws_bytes,
+             _stream_ptr(dev, stream)), (out, q, k_cache, v_cache, block_tables, context_lens, workspace))
+
+
+def decode_raw(args: tuple) -> None:
+    """Calls paged_decode_attention with arguments prepared by ``decode_args``."""
+    _check(_decode(*args[0]), "paged_decode_attention")
+
+
+def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           num_kv_heads: Optional[int] = None, *, max_context_len: Optional[int] = None,
+                           partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """out[s, hq] = softmax(scale * K_s q[s, hq]) V_s over context_lens[s] tokens
+    read through block_tables[s]; see include/pagedkv.h.
+
+    q, out: [S, Hq, D]; k_cache, v_cache: [NB, Hkv, 16, D] (bf16 or fp32,
+    all one dtype); block_tables int32 [S, maxB]; context_lens int32 [S].
+    ``max_context_len`` defaults to context_lens.max() (a device sync).
+    ``partition_tokens``: 0 automatic, -1 balanced (persistent kernel, bf16),
+    > 0 fixed partitions of that many tokens.
+    A caller-provided ``workspace`` must have been zero-filled once before
+    its first use; the library leaves it zero-filled after each call.
+    """
+    decode_raw(decode_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                           max_context_len=max_context_len, partition_tokens=partition_tokens, workspace=workspace,
+                           stream=stream))
     return out
 
 

@@ -20,8 +20,32 @@ namespace {
 constexpr int kVersion = 100;          // 0.1.0
 constexpr int kDefaultPartition = 512; // tokens per split-context partition (32 blocks)
 constexpr int kMaxParts = 8192;        // partitions per sequence the reduce kernel handles
-constexpr int kNstage = 8;
-constexpr int kNcw = 4;
+// Launch shapes (compile-time; -D overrides are for tuning sweeps).
+#ifndef PKV_GRID_STAGES
+#define PKV_GRID_STAGES 8
+#endif
+#ifndef PKV_GRID_CONSUMERS
+#define PKV_GRID_CONSUMERS 4
+#endif
+#ifndef PKV_PERSIST_WARPS
+#define PKV_PERSIST_WARPS 16
+#endif
+#ifndef PKV_PERSIST_STAGES_D128
+#define PKV_PERSIST_STAGES_D128 1
+#endif
+#ifndef PKV_PERSIST_STAGES_D64
+#define PKV_PERSIST_STAGES_D64 2
+#endif
+constexpr int kNstage = PKV_GRID_STAGES;
+constexpr int kNcw = PKV_GRID_CONSUMERS;
+// persistent bf16 kernel: one CTA of kPersistWarps warps per SM
+constexpr int kPersistWarps = PKV_PERSIST_WARPS;
+constexpr int kPersistMaxCtas = 160;     // sizes the workspace; GB300 has 152 SMs
+#ifndef PKV_PERSIST_MAX_SEQS
+#define PKV_PERSIST_MAX_SEQS 8192
+#endif
+constexpr int kPersistMaxSeqs = PKV_PERSIST_MAX_SEQS;  // block-count prefix sums live in shared memory
+constexpr size_t kSmemLimit = 232448;    // 227 KiB per CTA
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -49,17 +73,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D view of a cache as rows of head_dim bf16: row = (block * Hkv + head) * 16
-// + slot. Box = 16 rows x 64 elements (one 128-byte swizzle span), so a
-// (block, head) tile of head_dim 128 is two boxes.
+// 4-D view of a cache that makes one TMA box of each (block, kv head) tile:
+// x = element within a 64-element (128-byte) half row, y = slot (16, stride
+// one row), z = which half of the row (head_dim / 64, stride 128 bytes),
+// w = (block * Hkv + head) tile. The box {64, 16, head_dim / 64, 1} is the
+// whole contiguous tile, landing in shared memory as [half][slot][64] with
+// the 128-byte swizzle on each 128-byte row. Loading from y = valid - 16
+// makes TMA zero-fill the rows before the tile start: that is how the last
+// block of a sequence arrives with its slots past the end already zero.
 int encode_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int num_kv_heads, int head_dim) {
     auto fn = encode_fn();
     if (!fn) return PKV_ERR_CUDA;
-    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)num_blocks * num_kv_heads * 16};
-    cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-    cuuint32_t box[2] = {64, 16};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(cache), dims, strides, box, estr,
+    cuuint64_t dims[4] = {64, 16, (cuuint64_t)head_dim / 64, (cuuint64_t)num_blocks * num_kv_heads};
+    cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, 128, (cuuint64_t)head_dim * 2 * 16};
+    cuuint32_t box[4] = {64, 16, (cuuint32_t)head_dim / 64, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
@@ -105,6 +134,80 @@ int launch_reduce(const pkv::DecodeParams &p, pkv_dtype dt, cudaStream_t st) {
     return check_launch();
 }
 
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t grid_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_context_len, int pt) {
+    const int mp = max_parts_for(max_context_len, pt);
+    if (mp <= 1) return 0;
+    return (size_t)num_seqs * num_q_heads * mp * (2 + (size_t)head_dim) * sizeof(float);
+}
+
+// Arrival counters [S][Hkv] (zero between calls), then one (max, sum, acc)
+// state per group head for up to two cut segments per warp.
+size_t persist_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
+    const int g = num_q_heads / num_kv_heads;
+    return align256((size_t)num_seqs * num_kv_heads * sizeof(int)) +
+           (size_t)kPersistMaxCtas * kPersistWarps * 2 * g * (2 + (size_t)head_dim) * sizeof(float);
+}
+
+int sm_count(int *n) {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) {
+        *n = cached[dev];
+        return PKV_OK;
+    }
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return PKV_ERR_CUDA;
+    if (dev >= 0 && dev < 64) cached[dev] = v;
+    *n = v;
+    return PKV_OK;
+}
+
+template <int D, int NT, int NS>
+int launch_persistent(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, cudaStream_t st) {
+    using C = pkv::PersistCfg<D, NT, NS, kPersistWarps>;
+    static_assert(C::smem_bytes(kPersistMaxSeqs) + 64 <= kSmemLimit, "persistent kernel exceeds shared memory");
+    auto kern = pkv::decode_bf16_persistent_kernel<D, NT, NS, kPersistWarps>;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const size_t max_smem = C::smem_bytes(kPersistMaxSeqs);
+    if (configured_device != dev) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured_device = dev;
+    }
+    int sms = 0;
+    if (sm_count(&sms) != PKV_OK) return PKV_ERR_CUDA;
+    const int grid = sms < kPersistMaxCtas ? sms : kPersistMaxCtas;
+    kern<<<grid, C::kThreads, C::smem_bytes(p.num_seqs), st>>>(tmk, tmv, p);
+    return check_launch();
+}
+
+// The persistent balanced kernel is chosen for bf16 when asked for
+// (PKV_PARTITION_BALANCED), or automatically (partition_tokens == 0) when
+// the batch has at least a quarter as many (sequence, kv head) units as the
+// GPU has persistent warps; with fewer, longer units the balanced split would
+// cut each unit into many segments, and 512-token partitions merged by the
+// reduce kernel are faster.
+bool use_persistent(pkv_dtype dtype, int partition_tokens, int num_seqs, int num_kv_heads) {
+    if (dtype != PKV_BF16 || num_seqs > kPersistMaxSeqs) return false;
+    if (partition_tokens == PKV_PARTITION_BALANCED) return true;
+    if (partition_tokens != 0) return false;
+    int sms = 0;
+    if (sm_count(&sms) != PKV_OK) sms = kPersistMaxCtas;
+    const int workers = (sms < kPersistMaxCtas ? sms : kPersistMaxCtas) * kPersistWarps;
+    return (long long)num_seqs * num_kv_heads * 4 >= workers;
+}
+
+// Shared by both decode entry points once the workspace is known.
+int decode_dispatch(void *out, const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                    const int32_t *context_lens, float scale, int num_kv_heads, int num_seqs, int num_q_heads,
+                    int head_dim, int max_blocks_per_seq, int num_blocks, int max_context_len, pkv_dtype dtype,
+                    int partition_tokens, void *workspace, size_t workspace_bytes, void *stream);
 }  // namespace
 
 extern "C" {
@@ -130,17 +233,27 @@ int pkv_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_
     (void)num_kv_heads;
     (void)max_context_len;
     if (partition_tokens > 0) return partition_tokens;
-    return kDefaultPartition;
+    return kDefaultPartition;  // automatic or balanced: 512 wherever fixed partitions are used
 }
 
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_context_len,
                                   int partition_tokens) {
-    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+    if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
     const int pt = pkv_decode_partition_tokens(num_seqs, num_kv_heads, max_context_len, partition_tokens);
     if (pt <= 0 || pt % 16 != 0) return 0;
-    const int mp = max_parts_for(max_context_len, pt);
-    if (mp <= 1) return 0;
-    return (size_t)num_seqs * num_q_heads * mp * (2 + (size_t)head_dim) * sizeof(float);
+    const size_t grid_ws = grid_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, pt);
+    if (partition_tokens > 0 || num_q_heads % num_kv_heads != 0) return grid_ws;
+    const size_t pers = persist_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim);
+    return pers > grid_ws ? pers : grid_ws;
+}
+
+int pkv_decode_launches(int num_seqs, int num_kv_heads, int max_context_len, int partition_tokens, pkv_dtype dtype) {
+    if (num_seqs <= 0 || num_kv_heads <= 0) return 0;
+    if (partition_tokens < PKV_PARTITION_BALANCED) return 0;
+    if (use_persistent(dtype, partition_tokens, num_seqs, num_kv_heads)) return 1;
+    const int pt = pkv_decode_partition_tokens(num_seqs, 1, max_context_len, partition_tokens);
+    if (pt <= 0 || pt % 16 != 0) return 0;
+    return max_parts_for(max_context_len, pt) > 1 ? 2 : 1;
 }
 
 int paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -148,65 +261,9 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
                            int num_seqs, int num_q_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
                            int max_context_len, pkv_dtype dtype, int partition_tokens, void *workspace,
                            size_t workspace_bytes, void *stream) {
-    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
-        max_context_len < 0 || partition_tokens < 0)
-        return PKV_ERR_ARG;
-    if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
-    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-    if (num_q_heads % num_kv_heads != 0) return PKV_ERR_ARG;
-    const int g = num_q_heads / num_kv_heads;
-    if (g > 16) return PKV_ERR_UNSUPPORTED;
-    if (!std::isfinite(scale)) return PKV_ERR_ARG;
-    if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
-    if ((int64_t)num_blocks * num_kv_heads * 16 >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return PKV_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_ARG;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
-    const int pt = pkv_decode_partition_tokens(num_seqs, num_kv_heads, max_context_len, partition_tokens);
-    if (pt % 16 != 0) return PKV_ERR_ARG;
-    const int mp = max_parts_for(max_context_len, pt);
-    if (mp > kMaxParts) return PKV_ERR_UNSUPPORTED;
-    const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
-                                                   partition_tokens);
-    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PKV_ERR_WORKSPACE;
-
-    pkv::DecodeParams p{};
-    p.out = out;
-    p.q = q;
-    p.k_cache = k_cache;
-    p.v_cache = v_cache;
-    p.block_tables = block_tables;
-    p.context_lens = context_lens;
-    p.ws_ml = static_cast<float *>(workspace);
-    p.ws_o = need ? static_cast<float *>(workspace) + (size_t)num_seqs * num_q_heads * mp * 2 : nullptr;
-    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    p.num_seqs = num_seqs;
-    p.num_q_heads = num_q_heads;
-    p.num_kv_heads = num_kv_heads;
-    p.group = g;
-    p.max_blocks_per_seq = max_blocks_per_seq;
-    p.num_blocks = num_blocks;
-    p.max_context_len = max_context_len;
-    p.part_blocks = pt / 16;
-    p.max_parts = mp;
-
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    dim3 grid(mp, num_kv_heads, num_seqs);
-    int rc;
-    if (dtype == PKV_BF16) {
-        alignas(64) CUtensorMap tmk, tmv;
-        if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
-        if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
-        if (head_dim == 128)
-            rc = g <= 8 ? launch_bf16<128, 1>(tmk, tmv, p, grid, st) : launch_bf16<128, 2>(tmk, tmv, p, grid, st);
-        else
-            rc = g <= 8 ? launch_bf16<64, 1>(tmk, tmv, p, grid, st) : launch_bf16<64, 2>(tmk, tmv, p, grid, st);
-    } else {
-        rc = head_dim == 128 ? launch_f32<128>(p, grid, st) : launch_f32<64>(p, grid, st);
-    }
-    if (rc != PKV_OK) return rc;
-    if (mp > 1) rc = head_dim == 128 ? launch_reduce<128>(p, dtype, st) : launch_reduce<64>(p, dtype, st);
-    return rc;
+    return decode_dispatch(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads, num_seqs,
+                           num_q_heads, head_dim, max_blocks_per_seq, num_blocks, max_context_len, dtype,
+                           partition_tokens, workspace, workspace_bytes, stream);
 }
 
 int kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache, void *v_cache, int num_tokens,
@@ -218,9 +275,13 @@ int kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k
     if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_ARG;
     if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
     const int vec_per_row = head_dim * elem_bytes(dtype) / 16;
-    pkv::kv_append_kernel<<<num_tokens, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+    const long long total = (long long)num_tokens * num_kv_heads * vec_per_row;
+    const int threads = 256;
+    const long long blocks = (total + threads - 1) / threads;
+    if (blocks > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    pkv::kv_append_kernel<<<(unsigned)blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, static_cast<uint4 *>(k_cache),
-        static_cast<uint4 *>(v_cache), num_kv_heads, vec_per_row, num_blocks);
+        static_cast<uint4 *>(v_cache), num_tokens, num_kv_heads, vec_per_row, num_blocks);
     return check_launch();
 }
 
@@ -297,6 +358,93 @@ int pkv_device_error(uint32_t *value, int clear) {
 
 }  // extern "C"
 
+
+namespace {
+
+int decode_dispatch(void *out, const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                    const int32_t *context_lens, float scale, int num_kv_heads, int num_seqs, int num_q_heads,
+                    int head_dim, int max_blocks_per_seq, int num_blocks, int max_context_len, pkv_dtype dtype,
+                    int partition_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+        max_context_len < 0 || partition_tokens < PKV_PARTITION_BALANCED)
+        return PKV_ERR_ARG;
+    if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0) return PKV_ERR_ARG;
+    const int g = num_q_heads / num_kv_heads;
+    if (g > 16) return PKV_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return PKV_ERR_ARG;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)num_blocks * num_kv_heads * 16 >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+    const int pt = pkv_decode_partition_tokens(num_seqs, num_kv_heads, max_context_len, partition_tokens);
+    if (pt % 16 != 0) return PKV_ERR_ARG;
+    const int mp = max_parts_for(max_context_len, pt);
+    const bool persistent = use_persistent(dtype, partition_tokens, num_seqs, num_kv_heads);
+    if (!persistent && mp > kMaxParts) return PKV_ERR_UNSUPPORTED;
+    const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                                                   partition_tokens);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PKV_ERR_WORKSPACE;
+
+    pkv::DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = g;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.max_context_len = max_context_len;
+    p.part_blocks = pt / 16;
+    p.max_parts = mp;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (persistent) {
+        p.counters = static_cast<int *>(workspace);
+        p.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                               align256((size_t)num_seqs * num_kv_heads * sizeof(int)));
+        alignas(64) CUtensorMap tmk, tmv;
+        int rc;
+        if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
+        if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
+        constexpr int ns128 = PKV_PERSIST_STAGES_D128, ns64 = PKV_PERSIST_STAGES_D64;
+        if (head_dim == 128)
+            return g <= 8 ? launch_persistent<128, 1, ns128>(tmk, tmv, p, st)
+                          : launch_persistent<128, 2, ns128>(tmk, tmv, p, st);
+        return g <= 8 ? launch_persistent<64, 1, ns64>(tmk, tmv, p, st) : launch_persistent<64, 2, ns64>(tmk, tmv, p, st);
+    }
+
+    const size_t grid_ws = grid_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, pt);
+    p.ws_ml = grid_ws ? static_cast<float *>(workspace) : nullptr;
+    p.ws_o = grid_ws ? static_cast<float *>(workspace) + (size_t)num_seqs * num_q_heads * mp * 2 : nullptr;
+    dim3 grid(mp, num_kv_heads, num_seqs);
+    int rc;
+    if (dtype == PKV_BF16) {
+        alignas(64) CUtensorMap tmk, tmv;
+        if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
+        if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
+        if (head_dim == 128)
+            rc = g <= 8 ? launch_bf16<128, 1>(tmk, tmv, p, grid, st) : launch_bf16<128, 2>(tmk, tmv, p, grid, st);
+        else
+            rc = g <= 8 ? launch_bf16<64, 1>(tmk, tmv, p, grid, st) : launch_bf16<64, 2>(tmk, tmv, p, grid, st);
+    } else {
+        rc = head_dim == 128 ? launch_f32<128>(p, grid, st) : launch_f32<64>(p, grid, st);
+    }
+    if (rc != PKV_OK) return rc;
+    if (mp > 1) rc = head_dim == 128 ? launch_reduce<128>(p, dtype, st) : launch_reduce<64>(p, dtype, st);
+    return rc;
+}
+
+}  // namespace
+
 // ---------------------------------------------------------------------------
 // Decode without a caller-provided workspace (see pagedkv.h): the scratch is a
 // file-scope device array whose device address is looked up once per device.
@@ -334,68 +482,18 @@ extern "C" int paged_decode_attention_static_workspace(void *out, const void *q,
                                                        int num_seqs, int num_q_heads, int head_dim,
                                                        int max_blocks_per_seq, int num_blocks, int max_context_len,
                                                        pkv_dtype dtype, int partition_tokens, void *stream) {
-    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
-        max_context_len < 0 || partition_tokens < 0)
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
+        partition_tokens < PKV_PARTITION_BALANCED)
         return PKV_ERR_ARG;
-    if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
-    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-    if (num_q_heads % num_kv_heads != 0) return PKV_ERR_ARG;
-    const int g = num_q_heads / num_kv_heads;
-    if (g > 16) return PKV_ERR_UNSUPPORTED;
-    if (!std::isfinite(scale)) return PKV_ERR_ARG;
-    if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
-    if ((int64_t)num_blocks * num_kv_heads * 16 >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return PKV_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_ARG;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
-    const int pt = pkv_decode_partition_tokens(num_seqs, num_kv_heads, max_context_len, partition_tokens);
-    if (pt % 16 != 0) return PKV_ERR_ARG;
-    const int mp = max_parts_for(max_context_len, pt);
-    if (mp > kMaxParts) return PKV_ERR_UNSUPPORTED;
     const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
                                                    partition_tokens);
     if (need > PKV_STATIC_WORKSPACE_BYTES) return PKV_ERR_WORKSPACE;
     void *workspace = nullptr;
-    if (need > 0) {
+    if (need > 0 && num_seqs > 0) {
         const int rc = static_workspace_address(&workspace);
         if (rc != PKV_OK) return rc;
     }
-
-    pkv::DecodeParams p{};
-    p.out = out;
-    p.q = q;
-    p.k_cache = k_cache;
-    p.v_cache = v_cache;
-    p.block_tables = block_tables;
-    p.context_lens = context_lens;
-    p.ws_ml = static_cast<float *>(workspace);
-    p.ws_o = need ? static_cast<float *>(workspace) + (size_t)num_seqs * num_q_heads * mp * 2 : nullptr;
-    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    p.num_seqs = num_seqs;
-    p.num_q_heads = num_q_heads;
-    p.num_kv_heads = num_kv_heads;
-    p.group = g;
-    p.max_blocks_per_seq = max_blocks_per_seq;
-    p.num_blocks = num_blocks;
-    p.max_context_len = max_context_len;
-    p.part_blocks = pt / 16;
-    p.max_parts = mp;
-
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    dim3 grid(mp, num_kv_heads, num_seqs);
-    int rc;
-    if (dtype == PKV_BF16) {
-        alignas(64) CUtensorMap tmk, tmv;
-        if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
-        if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
-        if (head_dim == 128)
-            rc = g <= 8 ? launch_bf16<128, 1>(tmk, tmv, p, grid, st) : launch_bf16<128, 2>(tmk, tmv, p, grid, st);
-        else
-            rc = g <= 8 ? launch_bf16<64, 1>(tmk, tmv, p, grid, st) : launch_bf16<64, 2>(tmk, tmv, p, grid, st);
-    } else {
-        rc = head_dim == 128 ? launch_f32<128>(p, grid, st) : launch_f32<64>(p, grid, st);
-    }
-    if (rc != PKV_OK) return rc;
-    if (mp > 1) rc = head_dim == 128 ? launch_reduce<128>(p, dtype, st) : launch_reduce<64>(p, dtype, st);
-    return rc;
+    return decode_dispatch(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads, num_seqs,
+                           num_q_heads, head_dim, max_blocks_per_seq, num_blocks, max_context_len, dtype,
+                           partition_tokens, workspace, workspace ? (size_t)PKV_STATIC_WORKSPACE_BYTES : 0, stream);
 }

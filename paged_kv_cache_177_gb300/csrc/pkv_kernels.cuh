@@ -45,6 +45,8 @@ struct DecodeParams {
     int max_blocks_per_seq, num_blocks, max_context_len;
     int part_blocks;              // blocks per split-context partition
     int max_parts;                // partitions allotted per (sequence, head) in the workspace
+    int *counters;                // persistent kernel: [S][Hkv] arrival counters, zero between calls
+    float *partials;              // persistent kernel: [workers][2][g][2 + D] segment states
 };
 
 // A sequence's usable length: negative lengths and lengths past the table or
@@ -60,22 +62,178 @@ __device__ __forceinline__ int seq_len(const DecodeParams &p, int s, bool flag) 
 }
 
 // =====================================================================================
-// K1 (bf16): one CTA per (split-context partition, kv head, sequence).
-//
-// Warp NCW is the producer: it reads the partition's block ids from the table
-// 32 at a time and, for each block, issues TMA loads of the (block, kv head)
-// K and V tiles -- [16 tokens][D] each, contiguous in HBM -- into a ring of
-// NSTAGE shared-memory stages (128-byte swizzle, so fragment loads are free
-// of bank conflicts). Warps 0..NCW-1 consume blocks round-robin; each keeps
-// its own online-softmax state for the g query heads of the group:
+// The per-block step shared by both bf16 decode kernels. One warp attends a
+// (block, kv head) tile already staged in shared memory (K and V, [16][D]
+// each, 128-byte swizzle) for the g query heads of the group:
 //   S^T[16 tok x 8 heads]  = K[16 x D] . Q^T[D x 8]       (mma m16n8k16, bf16)
 //   m' = max(m, max_t s_t);  p_t = 2^(s_t - m');  l = l 2^(m - m') + sum_t p_t
 //   O^T[D x 8 heads]      = O^T 2^(m - m') + V^T[D x 16] . P^T[16 x 8]
-// The query heads of a GQA group share every K/V tile: the tile is read from
-// HBM once per group, and the group (padded to 8 or 16) is the MMA's N.
-// At the end the consumer warps merge their states through shared memory and
-// either write the final output (single-partition sequence) or the
-// partition's (max, sum, output) for the log-sum-exp reduce.
+// The query heads of a GQA group share the tile, which is read from HBM once
+// per group; the group (padded to 8 or 16) is the MMA's N. Scores are kept in
+// the log2 domain (scale_log2 = scale log2 e). Lane (gq = lane/4, t4 = lane%4)
+// holds heads 2 t4, 2 t4 + 1 of each 8-wide n-tile.
+// =====================================================================================
+template <int D, int NT>
+struct WarpAttn {
+    static constexpr int kSteps = D / 16;
+    static constexpr int kSubBytes = kBlock * 128;      // 2 KiB: 16 rows of 64 bf16
+    static constexpr int kSub = D / 64;
+    float m[NT][2], l[NT][2];
+    float acc[kSteps][NT][4];
+    uint32_t qf[kSteps][NT][2];                          // Q^T as the MMA B operand
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            m[nt][0] = m[nt][1] = -INFINITY;
+            l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < kSteps; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+        }
+    }
+
+    // b0 = q[head gq][16kk + 2t4 .. +1], b1 = the same + 8; heads past g read as 0.
+    static __device__ __forceinline__ void load_q_frags(uint32_t (&f)[kSteps][NT][2], const __nv_bfloat16 *q_group,
+                                                        int g, int lane) {
+        const int gq = lane >> 2, t4 = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int hl = nt * 8 + gq;
+            const bool hv = hl < g;
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(q_group + (size_t)(hv ? hl : 0) * D);
+#pragma unroll
+            for (int kk = 0; kk < kSteps; ++kk) {
+                f[kk][nt][0] = hv ? __ldg(qrow + (16 * kk + 2 * t4) / 2) : 0u;
+                f[kk][nt][1] = hv ? __ldg(qrow + (16 * kk + 8 + 2 * t4) / 2) : 0u;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void load_q(const __nv_bfloat16 *q_group, int g, int lane) {
+        load_q_frags(qf, q_group, g, lane);
+    }
+
+    // Attends one staged tile: sk, sv = shared addresses of the K and V tiles.
+    // Rows below `lo` are not tokens of the sequence: the last block of a
+    // sequence with v valid tokens is loaded shifted down by lo = 16 - v rows,
+    // so its first lo rows arrive zero-filled (zero V rows cannot poison the
+    // product) and are masked out of the softmax here.
+    __device__ __forceinline__ void block(uint32_t sk, uint32_t sv, int lo, float scale_log2, int lane) {
+        float sc[NT][4];
+        scores(sk, sc, lane);
+        softmax_pv(sc, sv, lo, scale_log2, lane);
+    }
+
+    // S^T = K . Q^T for the 16 tokens of the staged K tile (two independent
+    // accumulation chains over the head dimension, summed at the end).
+    __device__ __forceinline__ void scores(uint32_t sk, float (&sc)[NT][4], int lane) const {
+        const int mi = lane >> 3, r8 = lane & 7;
+        float sb[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[nt][e] = sb[nt][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < kSteps; ++kk) {
+            const int u = kk >> 2;
+            const int row = r8 + (mi & 1) * 8;
+            const int chunk = (kk & 3) * 2 + (mi >> 1);
+            uint32_t a[4];
+            ldsm_x4(sk + u * kSubBytes + row * 128 + ((chunk ^ (row & 7)) << 4), a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (kk & 1)
+                    mma_bf16_16816(sb[nt], a, qf[kk][nt][0], qf[kk][nt][1]);
+                else
+                    mma_bf16_16816(sc[nt], a, qf[kk][nt][0], qf[kk][nt][1]);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[nt][e] += sb[nt][e];
+    }
+
+    // Online-softmax update with the block's scores, then O^T += V^T . P^T
+    // from the staged V tile.
+    __device__ __forceinline__ void softmax_pv(const float (&sc)[NT][4], uint32_t sv, int lo, float scale_log2,
+                                               int lane) {
+        const int gq = lane >> 2;
+        const int mi = lane >> 3, r8 = lane & 7;
+        const bool v0 = gq >= lo, v1 = gq + 8 >= lo;
+        uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const float x0 = v0 ? sc[nt][0] * scale_log2 : -INFINITY;
+            const float x1 = v0 ? sc[nt][1] * scale_log2 : -INFINITY;
+            const float x2 = v1 ? sc[nt][2] * scale_log2 : -INFINITY;
+            const float x3 = v1 ? sc[nt][3] * scale_log2 : -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+            const float al0 = ex2_approx(m[nt][0] - mn0), al1 = ex2_approx(m[nt][1] - mn1);
+            m[nt][0] = mn0;
+            m[nt][1] = mn1;
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(ex2_approx(x0 - mn0), ex2_approx(x1 - mn1));
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(ex2_approx(x2 - mn0), ex2_approx(x3 - mn1));
+            const float2 flo = __bfloat1622float2(lo), fhi = __bfloat1622float2(hi);
+            // the sum uses the rounded weights the PV product uses, so they stay normalised
+            l[nt][0] = l[nt][0] * al0 + (flo.x + fhi.x);
+            l[nt][1] = l[nt][1] * al1 + (flo.y + fhi.y);
+#pragma unroll
+            for (int mt = 0; mt < kSteps; ++mt) {
+                acc[mt][nt][0] *= al0;
+                acc[mt][nt][1] *= al1;
+                acc[mt][nt][2] *= al0;
+                acc[mt][nt][3] *= al1;
+            }
+            // P^T as the B operand of PV: transpose the (token x head) 8x8 quads
+            pb0[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&lo));
+            pb1[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&hi));
+        }
+
+#pragma unroll
+        for (int mt = 0; mt < kSteps; ++mt) {
+            const int u = mt >> 2;
+            const int row = r8 + (mi >> 1) * 8;
+            const int chunk = (mt & 3) * 2 + (mi & 1);
+            uint32_t a[4];
+            ldsm_x4_trans(sv + u * kSubBytes + row * 128 + ((chunk ^ (row & 7)) << 4), a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a, pb0[nt], pb1[nt]);
+        }
+    }
+
+    // Sums l over the 8 lanes that share each head column.
+    __device__ __forceinline__ void reduce_l() {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) l[nt][c] += __shfl_xor_sync(0xffffffffu, l[nt][c], o);
+    }
+};
+
+// =====================================================================================
+// K1 (bf16, grid): one CTA per (split-context partition, kv head, sequence).
+//
+// Warp NCW is the producer: it reads the partition's block ids from the table
+// 32 at a time and, for each block, issues TMA loads of the (block, kv head)
+// K and V tiles -- [16 tokens][D] each, contiguous in HBM, one box each -- into a ring of
+// NSTAGE shared-memory stages (128-byte swizzle, so fragment loads are free
+// of bank conflicts). Warps 0..NCW-1 consume blocks round-robin, each with its
+// own online-softmax state (WarpAttn). At the end the consumer warps merge
+// their states through shared memory and either write the final output
+// (single-partition sequence) or the partition's (max, sum, output) for the
+// log-sum-exp reduce. Used for explicit partition sizes (and for batches
+// larger than the persistent kernel's table of sequences).
 // =====================================================================================
 template <int D, int NT, int NSTAGE, int NCW>
 struct Bf16Cfg {
@@ -153,20 +311,19 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
                         ok = false;
                     }
                     if (ok) {
-                        int y;
+                        int z;
                         if (pb < 0 || pb >= p.num_blocks) {
                             raise_error(PKV_DEVERR_BLOCK_ID);
-                            y = -kBlock;  // wholly outside the tensor: the tile reads as zeros
+                            z = -1;  // outside the tensor: the tile reads as zeros
                         } else {
-                            y = (pb * p.num_kv_heads + h) * kBlock;
+                            z = pb * p.num_kv_heads + h;
                         }
+                        // the sequence's last block: start last_valid - 16 rows early (zero fill)
+                        const int y = (b_begin + j == nblk - 1) ? last_valid - kBlock : 0;
                         mbar_arrive_expect_tx(&full[st], C::kStage);
                         uint8_t *sk = base + st * C::kStage;
-#pragma unroll
-                        for (int u = 0; u < C::kSub; ++u) tma_load_2d(sk + u * C::kSubBytes, &tmk, u * 64, y, &full[st]);
-#pragma unroll
-                        for (int u = 0; u < C::kSub; ++u)
-                            tma_load_2d(sk + C::kTile + u * C::kSubBytes, &tmv, u * 64, y, &full[st]);
+                        tma_load_4d(sk, &tmk, 0, y, 0, z, &full[st]);
+                        tma_load_4d(sk + C::kTile, &tmv, 0, y, 0, z, &full[st]);
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -178,34 +335,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
 
     // ------------------------------ consumers ------------------------------
     const int gq = lane >> 2, t4 = lane & 3;
-    // Q^T as the B operand of QK^T: b0 = q[head gq][16kk + 2t4 .. +1], b1 = same + 8.
-    uint32_t qf[C::kSteps][NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int hl = nt * 8 + gq;
-        const bool hv = hl < g;
-        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-            static_cast<const __nv_bfloat16 *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)h * g + (hv ? hl : 0)) * D);
-#pragma unroll
-        for (int kk = 0; kk < C::kSteps; ++kk) {
-            qf[kk][nt][0] = hv ? __ldg(qrow + (16 * kk + 2 * t4) / 2) : 0u;
-            qf[kk][nt][1] = hv ? __ldg(qrow + (16 * kk + 8 + 2 * t4) / 2) : 0u;
-        }
-    }
-
-    float m_run[NT][2], l_run[NT][2];
-    float acc[C::kSteps][NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        m_run[nt][0] = m_run[nt][1] = -INFINITY;
-        l_run[nt][0] = l_run[nt][1] = 0.f;
-#pragma unroll
-        for (int mt = 0; mt < C::kSteps; ++mt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
-    }
-
-    const int mi = lane >> 3, r8 = lane & 7;
+    WarpAttn<D, NT> wa;
+    wa.load_q(static_cast<const __nv_bfloat16 *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)h * g) * D, g, lane);
+    wa.reset();
     for (int j = warp; j < nb; j += NCW) {
         const int st = j % NSTAGE;
         if (!mbar_wait(&full[st], (j / NSTAGE) & 1)) {
@@ -213,96 +345,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
             break;
         }
         const uint32_t sk = smem_u32(base + st * C::kStage);
-        const uint32_t sv = sk + C::kTile;
-        const int valid = (b_begin + j == nblk - 1) ? last_valid : kBlock;
-
-        // S^T = K . Q^T  (rows: the block's 16 tokens; columns: the group's heads)
-        float sc[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < C::kSteps; ++kk) {
-            const int u = kk >> 2;
-            const int row = r8 + (mi & 1) * 8;
-            const int chunk = (kk & 3) * 2 + (mi >> 1);
-            uint32_t a[4];
-            ldsm_x4(sk + u * C::kSubBytes + row * 128 + ((chunk ^ (row & 7)) << 4), a);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[nt], a, qf[kk][nt][0], qf[kk][nt][1]);
-        }
-
-        // online softmax (log2 domain); tokens past the sequence end get -inf
-        const bool v0 = gq < valid, v1 = gq + 8 < valid;
-        uint32_t pb0[NT], pb1[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const float x0 = v0 ? sc[nt][0] * p.scale_log2 : -INFINITY;
-            const float x1 = v0 ? sc[nt][1] * p.scale_log2 : -INFINITY;
-            const float x2 = v1 ? sc[nt][2] * p.scale_log2 : -INFINITY;
-            const float x3 = v1 ? sc[nt][3] * p.scale_log2 : -INFINITY;
-            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            }
-            const float mn0 = fmaxf(m_run[nt][0], mx0), mn1 = fmaxf(m_run[nt][1], mx1);
-            const float al0 = ex2_approx(m_run[nt][0] - mn0), al1 = ex2_approx(m_run[nt][1] - mn1);
-            m_run[nt][0] = mn0;
-            m_run[nt][1] = mn1;
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(ex2_approx(x0 - mn0), ex2_approx(x1 - mn1));
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(ex2_approx(x2 - mn0), ex2_approx(x3 - mn1));
-            const float2 flo = __bfloat1622float2(lo), fhi = __bfloat1622float2(hi);
-            // the sum uses the rounded weights the PV product uses, so they stay normalised
-            l_run[nt][0] = l_run[nt][0] * al0 + (flo.x + fhi.x);
-            l_run[nt][1] = l_run[nt][1] * al1 + (flo.y + fhi.y);
-#pragma unroll
-            for (int mt = 0; mt < C::kSteps; ++mt) {
-                acc[mt][nt][0] *= al0;
-                acc[mt][nt][1] *= al1;
-                acc[mt][nt][2] *= al0;
-                acc[mt][nt][3] *= al1;
-            }
-            // P^T as the B operand of PV: transpose the (token x head) 8x8 quads
-            pb0[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&lo));
-            pb1[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&hi));
-        }
-
-        // V rows past the sequence end may hold anything (even NaN): zero them so
-        // that 0-weight * V cannot poison the product
-        if (valid < kBlock) {
-            const int nrow = kBlock - valid;
-            for (int i = lane; i < nrow * 8 * C::kSub; i += 32) {
-                const int u = i / (nrow * 8), rem = i % (nrow * 8);
-                st_shared_zero16(sv + u * C::kSubBytes + (valid + rem / 8) * 128 + (rem % 8) * 16);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        }
-
-        // O^T += V^T . P^T  (rows: head-dim, 16 per m-tile; columns: heads)
-#pragma unroll
-        for (int mt = 0; mt < C::kSteps; ++mt) {
-            const int u = mt >> 2;
-            const int row = r8 + (mi >> 1) * 8;
-            const int chunk = (mt & 3) * 2 + (mi & 1);
-            uint32_t a[4];
-            ldsm_x4_trans(sv + u * C::kSubBytes + row * 128 + ((chunk ^ (row & 7)) << 4), a);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[mt][nt], a, pb0[nt], pb1[nt]);
-        }
+        const int lo = (b_begin + j == nblk - 1) ? kBlock - last_valid : 0;
+        wa.block(sk, sk + C::kTile, lo, p.scale_log2, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
     }
 
     // ---------------- merge the consumer warps' states ----------------
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) l_run[nt][c] += __shfl_xor_sync(0xffffffffu, l_run[nt][c], o);
-
+    wa.reduce_l();
     named_barrier_sync(1, NCW * 32);  // every consumer is done with the stage ring
     float *mml = reinterpret_cast<float *>(base);                    // [NCW][kHeads][2]
     float *macc = mml + NCW * C::kHeads * 2;                         // [NCW][kHeads][kMergeStride]
@@ -312,8 +362,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int head = nt * 8 + 2 * t4 + c;
-                mml[(warp * C::kHeads + head) * 2 + 0] = m_run[nt][c];
-                mml[(warp * C::kHeads + head) * 2 + 1] = l_run[nt][c];
+                mml[(warp * C::kHeads + head) * 2 + 0] = wa.m[nt][c];
+                mml[(warp * C::kHeads + head) * 2 + 1] = wa.l[nt][c];
             }
     }
 #pragma unroll
@@ -324,7 +374,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
             for (int e = 0; e < 4; ++e) {
                 const int head = nt * 8 + 2 * t4 + (e & 1);
                 const int d = 16 * mt + gq + (e >> 1) * 8;
-                macc[(warp * C::kHeads + head) * C::kMergeStride + d] = acc[mt][nt][e];
+                macc[(warp * C::kHeads + head) * C::kMergeStride + d] = wa.acc[mt][nt][e];
             }
     named_barrier_sync(1, NCW * 32);
 
@@ -353,6 +403,390 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
                 p.ws_ml[r * 2 + 1] = L;
             }
         }
+    }
+}
+
+// =====================================================================================
+// K1 (bf16, persistent): one CTA per SM, NW warps, each warp an independent
+// decode worker with its own NS-stage TMA ring.
+//
+// All (sequence, kv head) units' blocks form one sequence of positions
+// (sequence-major, then head, then block); the T positions are cut into W
+// equal ranges, one per warp, so every warp streams the same number of K/V
+// tiles whatever the length mix. A warp walks its range block by block --
+// lane 0 keeps the ring NS blocks ahead with TMA, the lanes gather the block
+// ids of the next 32 positions ahead of use -- and keeps one online-softmax
+// state per unit segment. A unit that lies inside one range is written out
+// directly. A unit cut by range boundaries leaves one (max, sum, acc) state
+// per segment in the workspace; the warp that finishes the unit's last
+// outstanding segment (an arrival counter per unit) merges the segments with
+// the log-sum-exp rule in segment order and writes the output, so the result
+// does not depend on which warp arrives last.
+// =====================================================================================
+template <int D, int NT, int NS, int NW>
+struct PersistCfg {
+    static constexpr int kSub = D / 64;
+    static constexpr int kSubBytes = kBlock * 128;
+    static constexpr int kTile = kBlock * D * 2;
+    static constexpr int kStage = 2 * kTile;
+    static constexpr int kSteps = D / 16;
+    static constexpr int kThreads = NW * 32;
+    static constexpr int kRing = NW * NS * kStage;
+    static constexpr int kBarOffset = kRing;                         // K-full then V-full barriers
+    static constexpr int kPrefixOffset = kBarOffset + 2 * NW * NS * 8;
+    static constexpr size_t smem_bytes(int num_seqs) { return kPrefixOffset + (size_t)(num_seqs + 1) * 4 + 1024; }
+};
+
+// Position cursor: sequence s (with n = its blocks), kv head h, block j.
+struct Cursor {
+    int s, h, j, n;
+};
+
+// Moves c forward by k >= 0 positions; prefix[] holds the block-count prefix
+// sums. The caller guarantees the target position exists.
+__device__ __forceinline__ void cursor_advance(Cursor &c, int k, const int *prefix, int num_kv_heads) {
+    while (c.j + k >= c.n) {
+        k -= c.n - c.j;
+        c.j = 0;
+        if (++c.h == num_kv_heads) {
+            c.h = 0;
+            do {
+                ++c.s;
+                c.n = prefix[c.s + 1] - prefix[c.s];
+            } while (c.n == 0);
+        }
+    }
+    c.j += k;
+}
+
+// Merges the nseg segment states of one cut unit (worker w1's second slot,
+// then the first slots of workers w1+1 ..) with the log-sum-exp rule and
+// writes the g output rows. One warp; lane k holds segment k's weights, and
+// every lane accumulates head-dim elements lane, lane+32, .. of all heads
+// with the loads of two segments in flight at a time.
+template <int D>
+__device__ __forceinline__ void merge_segments(const float *partials, size_t slot_floats, int w1, int nseg, int g,
+                                               __nv_bfloat16 *out_rows, int lane) {
+    constexpr int PER = D / 32;
+    auto seg_row = [&](int k, int head) -> const float * {
+        return partials + (size_t)(2 * (w1 + k) + (k == 0 ? 1 : 0)) * slot_floats + (size_t)head * (2 + D);
+    };
+    for (int head = 0; head < g; ++head) {
+        // M and L over all segments, 32 segments per pass
+        float M = -INFINITY;
+        for (int k0 = 0; k0 < nseg; k0 += 32) {
+            const float mk = (k0 + lane < nseg) ? __ldcg(seg_row(k0 + lane, head)) : -INFINITY;
+            M = fmaxf(M, mk);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float L = 0.f;
+        for (int k0 = 0; k0 < nseg; k0 += 32) {
+            const int k = k0 + lane;
+            if (k < nseg) {
+                const float *r = seg_row(k, head);
+                const float mk = __ldcg(r);
+                if (mk != -INFINITY) L += __ldcg(r + 1) * ex2_approx(mk - M);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        const float invL = 1.f / L;
+        float acc[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+        for (int k0 = 0; k0 < nseg; k0 += 32) {
+            const int kk = k0 + lane;
+            float ck = 0.f;
+            if (kk < nseg) {
+                const float mk = __ldcg(seg_row(kk, head));
+                ck = (mk == -INFINITY) ? 0.f : ex2_approx(mk - M) * invL;
+            }
+            const int nk = min(32, nseg - k0);
+            int k = 0;
+            for (; k + 2 <= nk; k += 2) {
+                const float c0 = __shfl_sync(0xffffffffu, ck, k), c1 = __shfl_sync(0xffffffffu, ck, k + 1);
+                const float *r0 = seg_row(k0 + k, head) + 2, *r1 = seg_row(k0 + k + 1, head) + 2;
+                float v0[PER], v1[PER];
+#pragma unroll
+                for (int i = 0; i < PER; ++i) {
+                    v0[i] = __ldcg(r0 + lane + 32 * i);
+                    v1[i] = __ldcg(r1 + lane + 32 * i);
+                }
+#pragma unroll
+                for (int i = 0; i < PER; ++i) acc[i] = fmaf(c0, v0[i], fmaf(c1, v1[i], acc[i]));
+            }
+            for (; k < nk; ++k) {
+                const float c0 = __shfl_sync(0xffffffffu, ck, k);
+                const float *r0 = seg_row(k0 + k, head) + 2;
+#pragma unroll
+                for (int i = 0; i < PER; ++i) acc[i] = fmaf(c0, __ldcg(r0 + lane + 32 * i), acc[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < PER; ++i) out_rows[(size_t)head * D + lane + 32 * i] = __float2bfloat16_rn(acc[i]);
+    }
+}
+
+template <int D, int NT, int NS, int NW>
+__global__ void __launch_bounds__(NW * 32, 1)
+    decode_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                                  const DecodeParams p) {
+    using C = PersistCfg<D, NT, NS, NW>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int warp_total[NW];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = p.num_seqs, Hkv = p.num_kv_heads, g = p.group;
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + C::kBarOffset);
+    int *prefix = reinterpret_cast<int *>(base + C::kPrefixOffset);
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+
+    if (tid == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+        for (int i = 0; i < 2 * NW * NS; ++i) mbar_init(&full[i], 1);
+        mbar_fence_init();
+    }
+
+    // ---- block-count prefix sums over the batch (every CTA computes its own copy) ----
+    const int per = (S + C::kThreads - 1) / C::kThreads;
+    const int s_lo = min(S, tid * per), s_hi = min(S, s_lo + per);
+    int local = 0;
+    for (int s = s_lo; s < s_hi; ++s) local += (seq_len(p, s, blockIdx.x == 0) + kBlock - 1) / kBlock;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_total[warp] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += warp_total[w];
+    for (int s = s_lo; s < s_hi; ++s) {
+        prefix[s] = run;
+        run += (seq_len(p, s, false) + kBlock - 1) / kBlock;
+    }
+    if (tid == 0) {
+        int tot = 0;
+        for (int w = 0; w < NW; ++w) tot += warp_total[w];
+        prefix[S] = tot;
+    }
+    __syncthreads();
+
+    // ---- empty contexts: zero output rows (spread over the CTAs) ----
+    for (int s = blockIdx.x; s < S; s += gridDim.x) {
+        if (prefix[s + 1] == prefix[s]) {
+            __nv_bfloat16 *o = out + (size_t)s * p.num_q_heads * D;
+            for (int i = tid; i < p.num_q_heads * D; i += C::kThreads) o[i] = __float2bfloat16_rn(0.f);
+        }
+    }
+
+    // ---- this warp's range of positions ----
+    // W = min(warps, T) workers, so every worker's range is non-empty and the
+    // workers covering a unit are consecutive
+    const long long T = (long long)Hkv * prefix[S];
+    const int W = (int)min((long long)gridDim.x * NW, T);
+    const int w = blockIdx.x * NW + warp;
+    if (w >= W) return;
+    const long long start = T * w / W, end = T * (w + 1) / W;
+    const int cnt = (int)(end - start);
+
+    Cursor c;
+    {
+        int lo = 0, hi = S - 1;  // largest s with Hkv * prefix[s] <= start (never an empty sequence)
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((long long)Hkv * prefix[mid] <= start) lo = mid; else hi = mid - 1;
+        }
+        c.s = lo;
+        c.n = prefix[lo + 1] - prefix[lo];
+        const int r = (int)(start - (long long)Hkv * prefix[lo]);
+        c.h = r / c.n;
+        c.j = r - c.h * c.n;
+    }
+
+    // Block ids of the 32 positions starting at cursor b (lane i: position b + i),
+    // and beside each, 16 * kv head + the rows its tile starts early (16 - valid
+    // tokens on a sequence's last block, else 0). Nothing here waits on the
+    // loads: they are checked when the position is issued, 32 blocks later.
+    struct Batch {
+        int pb, hs;
+    };
+    auto batch_of = [&](Cursor b, int count) -> Batch {
+        Batch r{0, 0};
+        if (lane < count) {
+            cursor_advance(b, lane, prefix, Hkv);
+            r.pb = __ldg(p.block_tables + (size_t)b.s * p.max_blocks_per_seq + b.j);
+            const int shift = (b.j == b.n - 1) ? kBlock * b.n - seq_len(p, b.s, false) : 0;
+            r.hs = b.h * 16 + shift;
+        }
+        return r;
+    };
+
+    uint64_t *kfull = full + warp * NS;
+    uint64_t *vfull = full + NW * NS + warp * NS;
+    uint8_t *ring = base + warp * NS * C::kStage;
+    Cursor bnext = c;
+    Batch cur = batch_of(c, min(32, cnt));
+    Batch nxt{0, 0};
+    if (cnt > 32) {
+        cursor_advance(bnext, 32, prefix, Hkv);
+        nxt = batch_of(bnext, min(32, cnt - 32));
+    }
+    // K and V of block b are issued separately (K first), both by lane 0.
+    int kissued = 0, vissued = 0;
+    int z_last = 0, y_last = 0;  // coordinates of the last K issued, reused by its V
+    auto issue_k = [&]() {
+        if (kissued > 0 && (kissued & 31) == 0) {
+            cur = nxt;
+            if (kissued + 32 < cnt) {
+                cursor_advance(bnext, 32, prefix, Hkv);
+                nxt = batch_of(bnext, min(32, cnt - kissued - 32));
+            }
+        }
+        const int pb = __shfl_sync(0xffffffffu, cur.pb, kissued & 31);
+        const int hs = __shfl_sync(0xffffffffu, cur.hs, kissued & 31);
+        if (lane == 0) {
+            if (pb < 0 || pb >= p.num_blocks) {
+                raise_error(PKV_DEVERR_BLOCK_ID);
+                z_last = -1;  // outside the tensor: the tile reads as zeros
+            } else {
+                z_last = pb * Hkv + (hs >> 4);
+            }
+            y_last = -(hs & 15);
+            const int st = kissued % NS;
+            mbar_arrive_expect_tx(&kfull[st], C::kTile);
+            uint8_t *sk = ring + st * C::kStage;
+            tma_load_4d(sk, &tmk, 0, y_last, 0, z_last, &kfull[st]);
+        }
+        ++kissued;
+    };
+    auto issue_v = [&]() {
+        if (lane == 0) {
+            const int st = vissued % NS;
+            mbar_arrive_expect_tx(&vfull[st], C::kTile);
+            uint8_t *sv = ring + st * C::kStage + C::kTile;
+            tma_load_4d(sv, &tmv, 0, y_last, 0, z_last, &vfull[st]);
+        }
+        ++vissued;
+    };
+    while (kissued < min(NS, cnt)) {
+        issue_k();
+        issue_v();
+    }
+
+    const int gq = lane >> 2, t4 = lane & 3;
+    const size_t slot_floats = (size_t)g * (2 + D);
+    WarpAttn<D, NT> wa;
+    int seg_j0 = c.j;
+    int len = seq_len(p, c.s, false);
+    wa.load_q(static_cast<const __nv_bfloat16 *>(p.q) + ((size_t)c.s * p.num_q_heads + (size_t)c.h * g) * D, g, lane);
+    wa.reset();
+
+    const __nv_bfloat16 *qbase = static_cast<const __nv_bfloat16 *>(p.q);
+    uint32_t qnext[C::kSteps][NT][2];
+    int len_next = 0;
+    for (int i = 0; i < cnt; ++i) {
+        const int st = i % NS;
+        const bool unit_end = c.j == c.n - 1;
+        Cursor cn = c;
+        if (unit_end && i != cnt - 1) {
+            // the next unit's query and length, in flight while this block computes
+            cursor_advance(cn, 1, prefix, Hkv);
+            WarpAttn<D, NT>::load_q_frags(qnext, qbase + ((size_t)cn.s * p.num_q_heads + (size_t)cn.h * g) * D, g,
+                                          lane);
+            len_next = seq_len(p, cn.s, false);
+        }
+        const uint32_t sk = smem_u32(ring + st * C::kStage);
+        const uint32_t par = (i / NS) & 1;
+        if (!mbar_wait(&kfull[st], par)) {
+            raise_error(PKV_DEVERR_TIMEOUT);
+            break;
+        }
+        float sc[NT][4];
+        wa.scores(sk, sc, lane);
+        __syncwarp();  // every lane's K fragment loads are done before the K refill
+        const bool refill = kissued < cnt;
+        if (refill) issue_k();
+        if (!mbar_wait(&vfull[st], par)) {
+            raise_error(PKV_DEVERR_TIMEOUT);
+            break;
+        }
+        wa.softmax_pv(sc, sk + C::kTile, unit_end ? kBlock * c.n - len : 0, p.scale_log2, lane);
+        __syncwarp();  // ... and its V fragment loads before the V refill
+        if (refill) issue_v();
+
+        if (!unit_end && i != cnt - 1) {
+            ++c.j;
+            continue;
+        }
+        // ---- the segment ends here ----
+        wa.reduce_l();
+        const size_t orow0 = (size_t)c.s * p.num_q_heads + (size_t)c.h * g;
+        if (seg_j0 == 0 && unit_end) {
+            // the whole unit: write the output from the fragments
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int head = nt * 8 + 2 * t4 + (e & 1);
+                    if (head < g) {
+                        const float inv = 1.f / wa.l[nt][e & 1];
+#pragma unroll
+                        for (int mt = 0; mt < C::kSteps; ++mt)
+                            out[(orow0 + head) * D + 16 * mt + gq + (e >> 1) * 8] =
+                                __float2bfloat16_rn(wa.acc[mt][nt][e] * inv);
+                    }
+                }
+        } else {
+            // a cut unit: leave this segment's state, then the last arrival merges
+            float *mine = p.partials + (size_t)(2 * w + (seg_j0 == 0 ? 1 : 0)) * slot_floats;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int head = nt * 8 + 2 * t4 + (e & 1);
+                    if (head < g) {
+                        float *row = mine + (size_t)head * (2 + D);
+                        if (gq == 0 && e < 2) {
+                            row[0] = wa.m[nt][e];
+                            row[1] = wa.l[nt][e];
+                        }
+#pragma unroll
+                        for (int mt = 0; mt < C::kSteps; ++mt) row[2 + 16 * mt + gq + (e >> 1) * 8] = wa.acc[mt][nt][e];
+                    }
+                }
+            __threadfence();
+            __syncwarp();
+            const int u = c.s * Hkv + c.h;
+            int prev = 0;
+            if (lane == 0) prev = atomicAdd(p.counters + u, 1);
+            prev = __shfl_sync(0xffffffffu, prev, 0);
+            const long long x0 = (long long)Hkv * prefix[c.s] + (long long)c.h * c.n;
+            const int w1 = (int)(((x0 + 1) * W - 1) / T);
+            const int w2 = (int)(((x0 + c.n) * W - 1) / T);
+            if (prev == w2 - w1) {
+                __threadfence();
+                merge_segments<D>(p.partials, slot_floats, w1, w2 - w1 + 1, g, out + orow0 * D, lane);
+                if (lane == 0) p.counters[u] = 0;  // ready for the next call
+            }
+        }
+        if (i == cnt - 1) break;
+        // ---- next unit ----
+        c = cn;
+        seg_j0 = 0;
+        len = len_next;
+#pragma unroll
+        for (int kk = 0; kk < C::kSteps; ++kk)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                wa.qf[kk][nt][0] = qnext[kk][nt][0];
+                wa.qf[kk][nt][1] = qnext[kk][nt][1];
+            }
+        wa.reset();
     }
 }
 
@@ -524,28 +958,27 @@ __global__ void __launch_bounds__(D) lse_reduce_kernel(const DecodeParams p) {
 }
 
 // =====================================================================================
-// K3: KV append. One CTA per token; 16-byte vectors over (kv head, head-dim).
+// K3: KV append. One thread per 16-byte vector of (token, kv head, head-dim
+// chunk), so even a one-token-per-sequence step spreads over many CTAs.
 // =====================================================================================
 __global__ void kv_append_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                                  const int64_t *__restrict__ slots, uint4 *__restrict__ kc, uint4 *__restrict__ vc,
-                                 int num_kv_heads, int vec_per_row, int num_blocks) {
-    const int t = blockIdx.x;
+                                 int num_tokens, int num_kv_heads, int vec_per_row, int num_blocks) {
+    const int per_token = num_kv_heads * vec_per_row;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)num_tokens * per_token) return;
+    const int t = (int)(idx / per_token);
+    const int rem = (int)(idx - (long long)t * per_token);
     const int64_t slot = __ldg(slots + t);
     if (slot < 0) return;
     if (slot >= (int64_t)num_blocks * kBlock) {
-        if (threadIdx.x == 0) raise_error(PKV_DEVERR_SLOT);
+        if (rem == 0) raise_error(PKV_DEVERR_SLOT);
         return;
     }
-    const int64_t blk = slot >> 4;
-    const int off = (int)(slot & 15);
-    const int n = num_kv_heads * vec_per_row;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const int hh = i / vec_per_row, c = i - hh * vec_per_row;
-        const size_t src = ((size_t)t * num_kv_heads + hh) * vec_per_row + c;
-        const size_t dst = (((size_t)blk * num_kv_heads + hh) * kBlock + off) * vec_per_row + c;
-        kc[dst] = __ldg(k + src);
-        vc[dst] = __ldg(v + src);
-    }
+    const int hh = rem / vec_per_row, c = rem - hh * vec_per_row;
+    const size_t dst = ((((size_t)(slot >> 4)) * num_kv_heads + hh) * kBlock + (slot & 15)) * vec_per_row + c;
+    kc[dst] = __ldg(k + idx);
+    vc[dst] = __ldg(v + idx);
 }
 
 // =====================================================================================

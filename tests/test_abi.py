@@ -83,6 +83,7 @@ def test_decode_rejects_bad_arguments_before_any_cuda_call(lib):
     assert _decode(lib, hq=8 * 17, hkv=8) == -2      # group of 17 > 16
     assert _decode(lib, hkv=0) == -1
     assert _decode(lib, S=-1) == -1
+    assert _decode(lib, pt=-2) == -1                 # below PKV_PARTITION_BALANCED
     assert _decode(lib, out=None) == -1              # null pointer
     assert _decode(lib, q=(1 << 12) + 4) == -7       # misaligned
     assert _decode(lib, pt=24) == -1                 # partition not a multiple of 16

@@ -64,7 +64,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("partition_tokens", [0, 16, 48, 128])
+@pytest.mark.parametrize("partition_tokens", [0, -1, 16, 48, 128])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_small_cases_all_partitions(case, partition_tokens):
     name, dt, hq, hkv, d = case
@@ -133,7 +133,7 @@ def test_step_on_a_side_stream_and_in_a_cuda_graph():
     ref = H.oracle_step(h, wc.layout, wc.scale)
     w = wc.to("cuda")
     lay = w.layout
-    ws = torch.empty(max(1, b.workspace_bytes(lay.spec.num_seqs, lay.spec.num_q_heads, lay.spec.num_kv_heads,
+    ws = torch.zeros(max(1, b.workspace_bytes(lay.spec.num_seqs, lay.spec.num_q_heads, lay.spec.num_kv_heads,
                                                 lay.spec.head_dim, lay.max_context_len, 64)),
                      dtype=torch.uint8, device="cuda")
     k0, v0 = w.k_cache.clone(), w.v_cache.clone()
@@ -241,3 +241,60 @@ def test_full_size_workload(name):
     assert torch.isfinite(o).all()
     vmax = torch.nan_to_num(w.v_cache.float(), nan=0.0).abs().max()
     assert float(o.abs().max()) <= float(vmax) * (1 + 1e-2)
+
+
+def test_persistent_path_leaves_counters_zero_and_repeats_bit_identically():
+    """bf16 with automatic partitioning runs the persistent balanced kernel:
+    its arrival counters return to zero after every call, and the merge of
+    cut sequences does not depend on which warp arrives last."""
+    b = H.lib()
+    for lens, hq, hkv in ((EDGE_LENGTHS, 16, 4), ((3000, 1, 2, 4000, 17), 64, 8), ((1, 1, 1), 8, 8)):
+        wc = W.make_workload("gqa8b", lengths_list=lens, num_q_heads=hq, num_kv_heads=hkv, seed=len(lens))
+        h = H.host_arrays(wc)
+        w = wc.to("cuda")
+        H.gpu_step(w, attention=False)
+        lay = w.layout
+        assert b.decode_launches(lay.spec.num_seqs, hkv, lay.max_context_len, -1, torch.bfloat16) == 1
+        need = b.workspace_bytes(lay.spec.num_seqs, hq, hkv, 128, lay.max_context_len, -1)
+        ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+        outs = []
+        for _ in range(3):
+            out = torch.empty_like(w.q)
+            b.paged_decode_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
+                                     max_context_len=lay.max_context_len, workspace=ws, partition_tokens=-1)
+            torch.cuda.synchronize()
+            counters = ws[: lay.spec.num_seqs * hkv * 4]
+            assert int(counters.count_nonzero()) == 0
+            outs.append(out)
+        assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+        ref = H.oracle_step(h, lay, w.scale)
+        H.assert_close(outs[0], ref, "bf16", f"persistent {lens}")
+
+
+def test_persistent_step_in_a_cuda_graph():
+    b = H.lib()
+    wc = W.make_workload("gqa8b", lengths_list=EDGE_LENGTHS, seed=21)
+    h = H.host_arrays(wc)
+    ref = H.oracle_step(h, wc.layout, wc.scale)
+    w = wc.to("cuda")
+    lay = w.layout
+    ws = torch.zeros(b.workspace_bytes(lay.spec.num_seqs, 32, 8, 128, lay.max_context_len, -1), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty_like(w.q)
+    s = torch.cuda.Stream()
+    H.gpu_step(w, attention=False)
+    torch.cuda.synchronize()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):     # first call outside capture
+        b.paged_decode_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
+                                 max_context_len=lay.max_context_len, workspace=ws, stream=s, partition_tokens=-1)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        b.paged_decode_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
+                                 max_context_len=lay.max_context_len, workspace=ws, stream=s, partition_tokens=-1)
+    for _ in range(3):
+        out.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        H.assert_close(out, ref, "bf16", "persistent graph replay")
