@@ -263,6 +263,26 @@ def run_reference(args, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def pack_inputs(tensors, dev):
+    """Packs tensors into one pinned host buffer and one device buffer (each
+    tensor 256-byte aligned); returns typed views into both and the buffers."""
+    offs, off = [], 0
+    for t in tensors:
+        offs.append(off)
+        off += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(max(off, 256), dtype=torch.uint8, pin_memory=True)
+    dev_buf = torch.empty(max(off, 256), dtype=torch.uint8, device=dev)
+    host_views, dev_views = [], []
+    for t, o in zip(tensors, offs):
+        nb = t.numel() * t.element_size()
+        hv = host_buf[o:o + nb].view(t.dtype).view(t.shape)
+        hv.copy_(t.cpu())
+        host_views.append(hv)
+        dev_views.append(dev_buf[o:o + nb].view(t.dtype).view(t.shape))
+    dev_buf.copy_(host_buf)
+    return host_views, dev_views, host_buf, dev_buf
+
+
 def run_ours(args, rank, world, local, dist):
     from paged_kv_cache_177_gb300 import build
     build.build_library()
@@ -289,9 +309,10 @@ def run_ours(args, rank, world, local, dist):
     # per-step inputs live in buffers of their own, so the end-to-end run can
     # refill them from pinned host memory; the step rewrites the same slots and
     # blocks every time, so repeating it is idempotent
-    host_in = [t.to("cpu").pin_memory() for t in (w.q, w.k_new, w.v_new, w.slot_mapping, w.block_tables,
-                                                 w.context_lens, w.cow_pairs)]
-    dev_in = [t.to(dev) for t in host_in]
+    # one step's inputs packed into one staging buffer (each 256-byte aligned):
+    # pinned on the host, and on the device, where the calls read typed views
+    host_in, dev_in, host_buf, dev_buf = pack_inputs(
+        [w.q, w.k_new, w.v_new, w.slot_mapping, w.block_tables, w.context_lens, w.cow_pairs], dev)
     q, k_new, v_new, slots, tables, lens, pairs = dev_in
     evict = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev).fill_(1.0)
 
@@ -377,9 +398,9 @@ def run_ours(args, rank, world, local, dist):
     value = total_bytes / t_step_max / 1e9
 
     # ---- end to end: per-step inputs copied in from pinned host memory and the
-    # output copied back, inside the timed region ----
+    # output copied back, inside the timed region (one copy each way) ----
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    h2d = host_buf.numel()
     d2h = host_out.numel() * host_out.element_size()
     e2e_steps = min(steps, 2000)
     eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(e2e_steps)]
@@ -388,8 +409,7 @@ def run_ours(args, rank, world, local, dist):
             flush_l2()
             if i >= args.warmup:
                 eev[i - args.warmup][0].record(stream)
-            for dst, src in zip(dev_in, host_in):
-                dst.copy_(src, non_blocking=True)
+            dev_buf.copy_(host_buf, non_blocking=True)
             g_step.replay()
             host_out.copy_(out, non_blocking=True)
             if i >= args.warmup:

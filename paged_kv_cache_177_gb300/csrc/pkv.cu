@@ -125,12 +125,13 @@ int launch_f32(const pkv::DecodeParams &p, dim3 grid, cudaStream_t st) {
 
 template <int D>
 int launch_reduce(const pkv::DecodeParams &p, pkv_dtype dt, cudaStream_t st) {
+    constexpr int PG = 512 / D;  // partition groups: 512 threads per row
     dim3 grid(p.num_q_heads, p.num_seqs);
-    const size_t smem = (32 + (size_t)p.max_parts) * sizeof(float);
+    const size_t smem = (32 + (size_t)PG * D + (size_t)p.max_parts) * sizeof(float);
     if (dt == PKV_BF16)
-        pkv::lse_reduce_kernel<__nv_bfloat16, D><<<grid, D, smem, st>>>(p);
+        pkv::lse_reduce_kernel<__nv_bfloat16, D, PG><<<grid, D * PG, smem, st>>>(p);
     else
-        pkv::lse_reduce_kernel<float, D><<<grid, D, smem, st>>>(p);
+        pkv::lse_reduce_kernel<float, D, PG><<<grid, D * PG, smem, st>>>(p);
     return check_launch();
 }
 

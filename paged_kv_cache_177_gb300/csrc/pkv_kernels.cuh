@@ -915,10 +915,12 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float *scrat
     return v;
 }
 
-template <typename OutT, int D>
-__global__ void __launch_bounds__(D) lse_reduce_kernel(const DecodeParams p) {
-    extern __shared__ float rsm[];  // [32] scratch + [max_parts] weights
+template <typename OutT, int D, int PG>
+__global__ void __launch_bounds__(D *PG) lse_reduce_kernel(const DecodeParams p) {
+    // PG groups of D threads: group k sums partitions k, k + PG, ...
+    extern __shared__ float rsm[];  // [32] scratch, [PG][D] group sums, [max_parts] weights
     const int hq = blockIdx.x, s = blockIdx.y, tid = threadIdx.x;
+    const int d = tid % D, grp = tid / D;
     const int len = seq_len(p, s, false);
     const int nblk = (len + kBlock - 1) / kBlock;
     const int npart = (nblk + p.part_blocks - 1) / p.part_blocks;
@@ -927,12 +929,13 @@ __global__ void __launch_bounds__(D) lse_reduce_kernel(const DecodeParams p) {
     const float *ml = p.ws_ml + row * p.max_parts * 2;
     const float *o = p.ws_o + row * p.max_parts * D;
     float *scratch = rsm;
-    float *w = rsm + 32;
+    float *gsum = rsm + 32;
+    float *w = gsum + PG * D;
     float M = -INFINITY;
-    for (int i = tid; i < npart; i += D) M = fmaxf(M, ml[2 * i]);
+    for (int i = tid; i < npart; i += D * PG) M = fmaxf(M, ml[2 * i]);
     M = block_reduce(M, true, scratch);
     float W = 0.f;
-    for (int i = tid; i < npart; i += D) {
+    for (int i = tid; i < npart; i += D * PG) {
         const float wi = ml[2 * i + 1] * exp2f(ml[2 * i] - M);
         w[i] = wi;
         W += wi;
@@ -940,20 +943,27 @@ __global__ void __launch_bounds__(D) lse_reduce_kernel(const DecodeParams p) {
     W = block_reduce(W, false, scratch);
     __syncthreads();
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    int i = 0;
-    for (; i + 4 <= npart; i += 4) {
-        a0 = fmaf(w[i + 0], o[(size_t)(i + 0) * D + tid], a0);
-        a1 = fmaf(w[i + 1], o[(size_t)(i + 1) * D + tid], a1);
-        a2 = fmaf(w[i + 2], o[(size_t)(i + 2) * D + tid], a2);
-        a3 = fmaf(w[i + 3], o[(size_t)(i + 3) * D + tid], a3);
+    int i = grp;
+    for (; i + 3 * PG < npart; i += 4 * PG) {
+        a0 = fmaf(w[i], o[(size_t)i * D + d], a0);
+        a1 = fmaf(w[i + PG], o[(size_t)(i + PG) * D + d], a1);
+        a2 = fmaf(w[i + 2 * PG], o[(size_t)(i + 2 * PG) * D + d], a2);
+        a3 = fmaf(w[i + 3 * PG], o[(size_t)(i + 3 * PG) * D + d], a3);
     }
-    for (; i < npart; ++i) a0 = fmaf(w[i], o[(size_t)i * D + tid], a0);
-    const float r = ((a0 + a1) + (a2 + a3)) / W;
-    OutT *out = static_cast<OutT *>(p.out);
-    if constexpr (sizeof(OutT) == 2) {
-        out[row * D + tid] = __float2bfloat16_rn(r);
-    } else {
-        out[row * D + tid] = r;
+    for (; i < npart; i += PG) a0 = fmaf(w[i], o[(size_t)i * D + d], a0);
+    gsum[grp * D + d] = (a0 + a1) + (a2 + a3);
+    __syncthreads();
+    if (grp == 0) {
+        float r = 0.f;
+#pragma unroll
+        for (int k = 0; k < PG; ++k) r += gsum[k * D + d];
+        r /= W;
+        OutT *out = static_cast<OutT *>(p.out);
+        if constexpr (sizeof(OutT) == 2) {
+            out[row * D + d] = __float2bfloat16_rn(r);
+        } else {
+            out[row * D + d] = r;
+        }
     }
 }
 
