@@ -483,6 +483,99 @@ def run_ours(args, rank, world, local, dist):
     print(json.dumps(line), flush=True)
 
 
+def run_op(args, rank, world, local, dist):
+    """Secondary measurements (one JSON line each, rank 0 only):
+    --op swap: swap-out (device pool -> pinned host pool) and swap-in (back to
+      fresh device blocks) of the blocks of a quarter of the workload's
+      sequences, as preemption does; GB/s of block bytes moved each way.
+    --op append_layers: kv_append of one token per sequence into every layer's
+      caches (40 layers) in one launch, against one launch per layer."""
+    from paged_kv_cache_177_gb300 import build
+    build.build_library()
+    from paged_kv_cache_177_gb300 import binding as B
+
+    if rank != 0:
+        return
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sp = W.spec(args.workload)
+    w = W.make_workload(sp, device=dev)
+    lay = w.layout
+    eb = 2 if sp.dtype == "bf16" else 4
+    block_bytes = sp.num_kv_heads * 16 * sp.head_dim * eb
+    evict = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev).fill_(1.0)
+    stream = torch.cuda.current_stream(dev)
+
+    def time_it(fn, n):
+        """Median device time of fn, captured once as a CUDA graph and replayed."""
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            fn()                                   # warm-up outside the capture
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            evict.sum()
+            evs[i][0].record(stream)
+            g.replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        t = sorted(a.elapsed_time(b) for a, b in evs)
+        return t[len(t) // 2] / 1e3
+
+    if args.op == "swap":
+        seqs = np.arange(0, sp.num_seqs, 4)
+        nblk = (lay.context_lens.astype(np.int64) + 15) // 16
+        blocks = np.concatenate([lay.block_tables[s, :nblk[s]] for s in seqs]).astype(np.int64)
+        n = len(blocks)
+        hk = torch.empty((n,) + tuple(w.k_cache.shape[1:]), dtype=w.k_cache.dtype, pin_memory=True)
+        hv = torch.empty_like(hk).pin_memory()
+        out_pairs = np.stack([blocks, np.arange(n)], 1)
+        back = np.random.default_rng(0).permutation(lay.num_blocks)[:n]
+        in_pairs = np.stack([np.arange(n), back], 1)
+        po, pi = torch.from_numpy(out_pairs).to(dev), torch.from_numpy(in_pairs).to(dev)
+        dk, dv = torch.empty_like(w.k_cache), torch.empty_like(w.v_cache)
+        B.check_swap_pairs(out_pairs, lay.num_blocks, n)
+        B.check_swap_pairs(in_pairs, n, lay.num_blocks)
+        t_out = time_it(lambda: B.swap_blocks(hk, hv, w.k_cache, w.v_cache, po, check=False), args.steps or 50)
+        t_in = time_it(lambda: B.swap_blocks(dk, dv, hk, hv, pi, check=False), args.steps or 50)
+        moved = 2 * n * block_bytes
+        line = {"metric": "swap_blocks GB/s (block bytes moved per direction)", "unit": "GB/s",
+                "value": round(moved / t_out / 1e9, 2),
+                "swap_out": {"GB/s": round(moved / t_out / 1e9, 2), "us": round(t_out * 1e6, 2)},
+                "swap_in": {"GB/s": round(moved / t_in / 1e9, 2), "us": round(t_in * 1e6, 2)},
+                "blocks": int(n), "bytes_per_direction": int(moved), "higher_is_better": True,
+                "config": {"workload": describe(sp), "host_pool": "pinned host memory addressed by the kernel"}}
+    else:
+        L = 40
+        T = sp.num_seqs
+        slots = w.slot_mapping
+        kn = [torch.randn(w.k_new.shape, device=dev).to(w.k_new.dtype) for _ in range(L)]
+        vn = [torch.randn(w.v_new.shape, device=dev).to(w.v_new.dtype) for _ in range(L)]
+        # L layers' caches: views of one pool cut into L equal block ranges; one
+        # token per sequence, each in a block of its own
+        per = lay.num_blocks // L
+        assert T <= per
+        slots = torch.arange(T, device=dev, dtype=torch.int64) * 16 + 3
+        kc = [w.k_cache[l * per:(l + 1) * per] for l in range(L)]
+        vc = [w.v_cache[l * per:(l + 1) * per] for l in range(L)]
+        ptrs = tuple(B.layer_pointers(x) for x in (kn, vn, kc, vc))
+        t_one = time_it(lambda: B.kv_append_layers(kn, vn, slots, kc, vc, ptrs=ptrs), args.steps or 50)
+        t_each = time_it(lambda: [B.kv_append(kn[l], vn[l], slots, kc[l], vc[l]) for l in range(L)], args.steps or 50)
+        moved = L * T * sp.num_kv_heads * sp.head_dim * eb * 2 * 2
+        line = {"metric": "kv_append over 40 layers, GB/s (read + write of the appended K/V)", "unit": "GB/s",
+                "value": round(moved / t_one / 1e9, 2),
+                "one_launch": {"GB/s": round(moved / t_one / 1e9, 2), "us": round(t_one * 1e6, 2)},
+                "one_launch_per_layer": {"GB/s": round(moved / t_each / 1e9, 2), "us": round(t_each * 1e6, 2)},
+                "timing": "each variant captured once as a CUDA graph and replayed",
+                "higher_is_better": True, "config": {"workload": describe(sp), "layers": L, "tokens": T}}
+    line.update({"op": args.op, "n_gpus": 1, "dtype": sp.dtype, "data": "synthetic"})
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -495,6 +588,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["step", "swap", "append_layers"], default="step",
+                    help="step: the decode step (the benchmark line); swap / append_layers: secondary measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -506,6 +601,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world, dist)
+        elif args.op != "step":
+            run_op(args, rank, world, local, dist)
         else:
             run_ours(args, rank, world, local, dist)
     finally:

@@ -76,6 +76,7 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_DEVERR_PAIR 0x4u        /* a copy pair outside [0, num_blocks): that pair was skipped */
 #define PKV_DEVERR_TIMEOUT 0x8u     /* a bounded wait inside a kernel ran out: output unspecified */
 #define PKV_DEVERR_LENGTH 0x10u     /* context_len < 0, > max_blocks_per_seq*16 or > max_context_len: clamped */
+#define PKV_DEVERR_POINTER 0x20u    /* a pointer in a per-layer pointer array is null or not 16-byte aligned: skipped */
 
 /* Human-readable name of a status code (static storage). */
 const char *pkv_status_string(int status);
@@ -163,6 +164,53 @@ int kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k
  */
 int copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs, int num_pairs, int num_kv_heads,
                 int head_dim, int num_blocks, pkv_dtype dtype, void *stream);
+
+/*
+ * Block swap between two pools ("Batching Continuo y PagedAttention",
+ * cruxr.ai, section "Juntándolo todo: Arquitectura de vLLM": under memory
+ * pressure the scheduler copies a low-priority request's KV blocks to CPU
+ * memory, frees the GPU blocks, and copies them back to resume). For each pair
+ * i, block src_dst_pairs[i][0] of the source pool is copied onto block
+ * src_dst_pairs[i][1] of the destination pool, all kv heads and 16 slots, in
+ * both caches. Each pool is [num_blocks][num_kv_heads][16][head_dim] in device
+ * memory or in pinned host memory the GPU can address (cudaHostAlloc or
+ * cudaHostRegister with unified addressing: the host pointer is used as is).
+ * src_dst_pairs: int64 [num_pairs][2] in device-accessible memory. Swap-out
+ * is device -> host pool, swap-in host -> device pool; device -> device moves
+ * between pools too. Destinations must be distinct (pkv_check_swap_pairs);
+ * pairs out of range are skipped and flagged (PKV_DEVERR_PAIR). Bit-exact.
+ */
+int swap_blocks(void *dst_k_cache, void *dst_v_cache, int dst_num_blocks, const void *src_k_cache,
+                const void *src_v_cache, int src_num_blocks, const int64_t *src_dst_pairs, int num_pairs,
+                int num_kv_heads, int head_dim, pkv_dtype dtype, void *stream);
+
+/*
+ * Host-side check of swap pairs (HOST pointer): PKV_ERR_INDEX if an id is
+ * outside its pool, PKV_ERR_OVERLAP if a destination repeats. No CUDA call.
+ */
+int pkv_check_swap_pairs(const int64_t *host_pairs, int num_pairs, int src_num_blocks, int dst_num_blocks);
+
+/*
+ * copy_blocks for num_layers layers in one launch: a logical block spans all
+ * layers ("Batching Continuo y PagedAttention", section "PagedAttention:
+ * Memoria virtual para la KV cache"), so one copy-on-write copies it in every
+ * layer's cache. k_caches, v_caches: arrays of num_layers cache pointers, the
+ * arrays themselves in device-accessible memory; every layer's pool has
+ * num_blocks blocks of the same shape. A null or misaligned pointer skips
+ * that layer (PKV_DEVERR_POINTER). Same pair rules as copy_blocks.
+ */
+int copy_blocks_layers(void *const *k_caches, void *const *v_caches, int num_layers, const int64_t *src_dst_pairs,
+                       int num_pairs, int num_kv_heads, int head_dim, int num_blocks, pkv_dtype dtype, void *stream);
+
+/*
+ * kv_append for num_layers layers in one launch: layer l writes k[l][t], v[l][t]
+ * ([num_tokens][num_kv_heads][head_dim]) into k_caches[l], v_caches[l] at
+ * slot_mapping[t] (one slot mapping for all layers). Pointer arrays in
+ * device-accessible memory; same slot rules as kv_append.
+ */
+int kv_append_layers(const void *const *k, const void *const *v, const int64_t *slot_mapping, void *const *k_caches,
+                     void *const *v_caches, int num_layers, int num_tokens, int num_kv_heads, int head_dim,
+                     int num_blocks, pkv_dtype dtype, void *stream);
 
 /*
  * Host-side check of copy pairs (HOST pointer, int64 [num_pairs][2]):

@@ -26,6 +26,7 @@ _lib = ctypes.CDLL(LIB)
 PKV_F32, PKV_BF16 = 0, 1
 PARTITION_AUTO, PARTITION_BALANCED = 0, -1
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_PAIR, DEVERR_TIMEOUT, DEVERR_LENGTH = 0x1, 0x2, 0x4, 0x8, 0x10
+DEVERR_POINTER = 0x20
 BLOCK_SIZE = 16
 
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -47,6 +48,10 @@ _decode = _decl("paged_decode_attention", _i, _vp, _vp, _vp, _vp, _vp, _vp, _f, 
                 _vp, _sz, _vp)
 _append = _decl("kv_append", _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
 _copy = _decl("copy_blocks", _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
+_swap = _decl("swap_blocks", _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp)
+_check_swap = _decl("pkv_check_swap_pairs", _i, _vp, _i, _i, _i)
+_copy_layers = _decl("copy_blocks_layers", _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _vp)
+_append_layers = _decl("kv_append_layers", _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp)
 _check_pairs = _decl("pkv_check_copy_pairs", _i, _vp, _i, _i)
 _validate = _decl("pkv_validate", _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp)
 _validate_slots = _decl("pkv_validate_slots", _i, _vp, _i, _i, _vp, _vp)
@@ -224,6 +229,116 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: tor
         check_copy_pairs(host_pairs if host_pairs is not None else src_dst_pairs.cpu().numpy(), NB)
     _check(_copy(_p(k_cache), _p(v_cache), _p(src_dst_pairs) if n else None, n, Hkv, D, NB, dt,
                  _stream_ptr(dev, stream)), "copy_blocks")
+
+
+def _pool_ok(t: torch.Tensor) -> None:
+    if not t.is_contiguous():
+        raise ValueError("pools must be contiguous")
+    if t.device.type != "cuda" and not t.is_pinned():
+        raise ValueError("a pool must be a CUDA tensor or pinned host memory")
+
+
+def check_swap_pairs(pairs, src_num_blocks: int, dst_num_blocks: int) -> None:
+    """Host-side range check of (src, dst) swap pairs and distinct destinations."""
+    arr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    _check(_check_swap(arr.ctypes.data if arr.size else None, arr.shape[0], int(src_num_blocks), int(dst_num_blocks)),
+           "swap_blocks pairs")
+
+
+def swap_blocks(dst_k: torch.Tensor, dst_v: torch.Tensor, src_k: torch.Tensor, src_v: torch.Tensor,
+                src_dst_pairs: torch.Tensor, *, host_pairs=None, check: bool = True,
+                stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copies block src of the source pool onto block dst of the destination
+    pool (both caches) for each pair.  A pool is a CUDA tensor or a pinned
+    host tensor [NB, Hkv, 16, D]; swap-out goes device -> host, swap-in host ->
+    device.  ``src_dst_pairs``: int64 [n, 2], on the device or pinned."""
+    for t in (dst_k, dst_v, src_k, src_v, src_dst_pairs):
+        _pool_ok(t)
+    if src_dst_pairs.dtype != torch.int64:
+        raise TypeError("src_dst_pairs must be int64")
+    if not (dst_k.dtype == dst_v.dtype == src_k.dtype == src_v.dtype):
+        raise TypeError("pools must share one dtype")
+    dt = _dtype_code(dst_k)
+    NBd, Hkv, P, D = dst_k.shape
+    NBs = src_k.shape[0]
+    if dst_v.shape != dst_k.shape or src_v.shape != src_k.shape or src_k.shape[1:] != dst_k.shape[1:] or P != BLOCK_SIZE:
+        raise ValueError("pools must be [NB, Hkv, 16, D] with matching block shapes")
+    n = src_dst_pairs.numel() // 2
+    if check:
+        check_swap_pairs(host_pairs if host_pairs is not None else src_dst_pairs.cpu().numpy(), NBs, NBd)
+    dev = next((t.device for t in (dst_k, src_k, src_dst_pairs) if t.device.type == "cuda"), None)
+    if dev is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    _check(_swap(_p(dst_k), _p(dst_v), NBd, _p(src_k), _p(src_v), NBs, _p(src_dst_pairs) if n else None, n, Hkv, D,
+                 dt, _stream_ptr(dev, stream)), "swap_blocks")
+
+
+def _ptr_array(ts, dev) -> torch.Tensor:
+    return torch.tensor([t.data_ptr() for t in ts], dtype=torch.int64, device=dev)
+
+
+def layer_pointers(tensors, device=None) -> torch.Tensor:
+    """A device array of the tensors' data pointers, for the per-layer calls.
+    Build it once and pass it back through ``ptrs=`` to keep the calls free of
+    host-to-device copies (for example inside CUDA graph capture); the tensors
+    must stay alive and in place while the array is used."""
+    dev = device if device is not None else tensors[0].device
+    return _ptr_array(tensors, dev)
+
+
+def copy_blocks_layers(k_caches, v_caches, src_dst_pairs: torch.Tensor, *, host_pairs=None, check: bool = True,
+                       stream: Optional[torch.cuda.Stream] = None, ptrs=None) -> None:
+    """copy_blocks over every layer's caches (lists of [NB, Hkv, 16, D] CUDA
+    tensors, one per layer) in one launch.  ``ptrs``: optional prebuilt
+    (k_caches, v_caches) pointer arrays from ``layer_pointers``."""
+    if len(k_caches) != len(v_caches):
+        raise ValueError("one K and one V cache per layer")
+    if not k_caches:
+        return
+    dev = _dev(*k_caches, *v_caches, src_dst_pairs)
+    dt = _dtype_code(k_caches[0])
+    shape = k_caches[0].shape
+    for t in (*k_caches, *v_caches):
+        if t.shape != shape or t.dtype != k_caches[0].dtype:
+            raise ValueError("every layer's caches must share shape and dtype")
+    NB, Hkv, P, D = shape
+    n = src_dst_pairs.numel() // 2
+    if check:
+        check_copy_pairs(host_pairs if host_pairs is not None else src_dst_pairs.cpu().numpy(), NB)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.stream(st):  # the pointer arrays are copied in on the launch stream
+        kp, vp = ptrs if ptrs is not None else (_ptr_array(k_caches, dev), _ptr_array(v_caches, dev))
+        _check(_copy_layers(_p(kp), _p(vp), len(k_caches), _p(src_dst_pairs) if n else None, n, Hkv, D, NB, dt,
+                            st.cuda_stream), "copy_blocks_layers")
+
+
+def kv_append_layers(ks, vs, slot_mapping: torch.Tensor, k_caches, v_caches, *,
+                     stream: Optional[torch.cuda.Stream] = None, ptrs=None) -> None:
+    """kv_append for every layer in one launch: layer l writes ks[l], vs[l]
+    ([T, Hkv, D]) into k_caches[l], v_caches[l] at the same slots.  ``ptrs``:
+    optional prebuilt (ks, vs, k_caches, v_caches) pointer arrays."""
+    L = len(k_caches)
+    if not (len(ks) == len(vs) == L == len(v_caches)):
+        raise ValueError("one k, v, K cache and V cache per layer")
+    if L == 0:
+        return
+    dev = _dev(*ks, *vs, *k_caches, *v_caches, slot_mapping)
+    dt = _dtype_code(k_caches[0])
+    T, Hkv, D = ks[0].shape
+    NB = k_caches[0].shape[0]
+    for t in (*ks, *vs):
+        if t.shape != (T, Hkv, D) or t.dtype != k_caches[0].dtype:
+            raise ValueError("every layer's k and v must be [T, Hkv, D] of the cache dtype")
+    for t in (*k_caches, *v_caches):
+        if t.shape != (NB, Hkv, BLOCK_SIZE, D) or t.dtype != k_caches[0].dtype:
+            raise ValueError("every layer's caches must be [NB, Hkv, 16, D]")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be int64 [T]")
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.stream(st):  # the pointer arrays are copied in on the launch stream
+        arrs = list(ptrs) if ptrs is not None else [_ptr_array(x, dev) for x in (ks, vs, k_caches, v_caches)]
+        _check(_append_layers(*(_p(a) for a in arrs[:2]), _p(slot_mapping), *(_p(a) for a in arrs[2:]), L, T, Hkv, D,
+                              NB, dt, st.cuda_stream), "kv_append_layers")
 
 
 def validate(block_tables: torch.Tensor, context_lens: torch.Tensor, num_blocks: int, max_context_len: int,

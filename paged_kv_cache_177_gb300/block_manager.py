@@ -137,6 +137,36 @@ class BlockManager:
         seq.length += 1
         return slot, cow
 
+    def swap_out(self, seq_id: int, host: "BlockManager") -> List[Tuple[int, int]]:
+        """Moves a sequence to a host pool (preemption by swapping, "Juntándolo
+        todo: Arquitectura de vLLM"): one host block per table entry, all or
+        nothing; returns the (device block, host block) pairs to copy, then
+        releases the device blocks (freed when no other table refers to
+        them). The sequence's length and table now live in ``host``."""
+        seq = self._seqs[seq_id]
+        if not host.can_allocate(len(seq.table)):
+            raise NoFreeBlocks(f"host pool: need {len(seq.table)} blocks, {host.num_free} free")
+        host_table = [host._alloc() for _ in seq.table]
+        host._seqs[seq_id] = _Seq(host_table, seq.length)
+        pairs = list(zip(seq.table, host_table))
+        self.free(seq_id)
+        return pairs
+
+    def swap_in(self, seq_id: int, host: "BlockManager") -> List[Tuple[int, int]]:
+        """Brings a swapped-out sequence back: fresh device blocks, all or
+        nothing; returns the (host block, device block) pairs to copy and
+        frees the host blocks."""
+        hseq = host._seqs[seq_id]
+        if seq_id in self._seqs:
+            raise ValueError(f"sequence {seq_id} is already resident")
+        if not self.can_allocate(len(hseq.table)):
+            raise NoFreeBlocks(f"need {len(hseq.table)} blocks, {self.num_free} free")
+        table = [self._alloc() for _ in hseq.table]
+        self._seqs[seq_id] = _Seq(table, hseq.length)
+        pairs = list(zip(hseq.table, table))
+        host.free(seq_id)
+        return pairs
+
     def free(self, seq_id: int) -> None:
         """Release all of a finished (or preempted) sequence's blocks."""
         seq = self._seqs.pop(seq_id)

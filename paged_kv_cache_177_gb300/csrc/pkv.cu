@@ -288,21 +288,92 @@ int kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k
 
 int copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs, int num_pairs, int num_kv_heads,
                 int head_dim, int num_blocks, pkv_dtype dtype, void *stream) {
-    if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_ARG;
+    return swap_blocks(k_cache, v_cache, num_blocks, k_cache, v_cache, num_blocks, src_dst_pairs, num_pairs,
+                       num_kv_heads, head_dim, dtype, stream);
+}
+
+int swap_blocks(void *dst_k_cache, void *dst_v_cache, int dst_num_blocks, const void *src_k_cache,
+                const void *src_v_cache, int src_num_blocks, const int64_t *src_dst_pairs, int num_pairs,
+                int num_kv_heads, int head_dim, pkv_dtype dtype, void *stream) {
+    if (num_pairs < 0 || num_kv_heads <= 0 || src_num_blocks <= 0 || dst_num_blocks <= 0) return PKV_ERR_ARG;
     if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (num_pairs == 0) return PKV_OK;
     if (num_pairs > 65535) return PKV_ERR_UNSUPPORTED;
-    if (!k_cache || !v_cache || !src_dst_pairs) return PKV_ERR_ARG;
-    if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
-    const int64_t vec_per_block = (int64_t)num_kv_heads * 16 * head_dim * elem_bytes(dtype) / 16;
+    if (!dst_k_cache || !dst_v_cache || !src_k_cache || !src_v_cache || !src_dst_pairs) return PKV_ERR_ARG;
+    if (!aligned16(dst_k_cache) || !aligned16(dst_v_cache) || !aligned16(src_k_cache) || !aligned16(src_v_cache))
+        return PKV_ERR_ALIGN;
+    pkv::BlockMove m{};
+    m.src[0] = static_cast<const uint4 *>(src_k_cache);
+    m.src[1] = static_cast<const uint4 *>(src_v_cache);
+    m.dst[0] = static_cast<uint4 *>(dst_k_cache);
+    m.dst[1] = static_cast<uint4 *>(dst_v_cache);
+    m.src_num_blocks = src_num_blocks;
+    m.dst_num_blocks = dst_num_blocks;
+    m.vec_per_block = (int64_t)num_kv_heads * 16 * head_dim * elem_bytes(dtype) / 16;
     const int threads = 256;
-    int64_t chunks = (vec_per_block + threads * 4 - 1) / (threads * 4);
+    int64_t chunks = (m.vec_per_block + threads * 4 - 1) / (threads * 4);
     if (chunks > 1024) chunks = 1024;
-    dim3 grid((unsigned)chunks, num_pairs, 2);
-    pkv::copy_blocks_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src_dst_pairs, num_blocks, vec_per_block);
+    pkv::move_blocks_kernel<<<dim3((unsigned)chunks, num_pairs, 2), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+        m, src_dst_pairs);
     return check_launch();
+}
+
+int copy_blocks_layers(void *const *k_caches, void *const *v_caches, int num_layers, const int64_t *src_dst_pairs,
+                       int num_pairs, int num_kv_heads, int head_dim, int num_blocks, pkv_dtype dtype, void *stream) {
+    if (num_pairs < 0 || num_layers < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_ARG;
+    if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_pairs == 0 || num_layers == 0) return PKV_OK;
+    if (num_pairs > 65535 || num_layers > 32767) return PKV_ERR_UNSUPPORTED;
+    if (!k_caches || !v_caches || !src_dst_pairs) return PKV_ERR_ARG;
+    pkv::BlockMove m{};
+    m.src_k_layers = reinterpret_cast<const uint4 *const *>(k_caches);
+    m.src_v_layers = reinterpret_cast<const uint4 *const *>(v_caches);
+    m.dst_k_layers = reinterpret_cast<uint4 *const *>(k_caches);
+    m.dst_v_layers = reinterpret_cast<uint4 *const *>(v_caches);
+    m.src_num_blocks = m.dst_num_blocks = num_blocks;
+    m.vec_per_block = (int64_t)num_kv_heads * 16 * head_dim * elem_bytes(dtype) / 16;
+    const int threads = 256;
+    int64_t chunks = (m.vec_per_block + threads * 4 - 1) / (threads * 4);
+    if (chunks > 1024) chunks = 1024;
+    pkv::move_blocks_kernel<<<dim3((unsigned)chunks, num_pairs, 2 * num_layers), threads, 0,
+                              static_cast<cudaStream_t>(stream)>>>(m, src_dst_pairs);
+    return check_launch();
+}
+
+int kv_append_layers(const void *const *k, const void *const *v, const int64_t *slot_mapping, void *const *k_caches,
+                     void *const *v_caches, int num_layers, int num_tokens, int num_kv_heads, int head_dim,
+                     int num_blocks, pkv_dtype dtype, void *stream) {
+    if (num_tokens < 0 || num_layers < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_ARG;
+    if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0 || num_layers == 0) return PKV_OK;
+    if (num_layers > 65535) return PKV_ERR_UNSUPPORTED;
+    if (!k || !v || !slot_mapping || !k_caches || !v_caches) return PKV_ERR_ARG;
+    const int vec_per_row = head_dim * elem_bytes(dtype) / 16;
+    const long long total = (long long)num_tokens * num_kv_heads * vec_per_row;
+    const int threads = 256;
+    const long long blocks = (total + threads - 1) / threads;
+    if (blocks > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    pkv::kv_append_layers_kernel<<<dim3((unsigned)blocks, num_layers), threads, 0,
+                                   static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const uint4 *const *>(k), reinterpret_cast<const uint4 *const *>(v), slot_mapping,
+        reinterpret_cast<uint4 *const *>(k_caches), reinterpret_cast<uint4 *const *>(v_caches), num_tokens,
+        num_kv_heads, vec_per_row, num_blocks);
+    return check_launch();
+}
+
+int pkv_check_swap_pairs(const int64_t *host_pairs, int num_pairs, int src_num_blocks, int dst_num_blocks) {
+    if (num_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0) return PKV_ERR_ARG;
+    if (num_pairs > 0 && !host_pairs) return PKV_ERR_ARG;
+    std::unordered_set<int64_t> dsts;
+    for (int i = 0; i < num_pairs; ++i) {
+        const int64_t s = host_pairs[2 * i], d = host_pairs[2 * i + 1];
+        if (s < 0 || s >= src_num_blocks || d < 0 || d >= dst_num_blocks) return PKV_ERR_INDEX;
+        if (!dsts.insert(d).second) return PKV_ERR_OVERLAP;
+    }
+    return PKV_OK;
 }
 
 int pkv_check_copy_pairs(const int64_t *host_pairs, int num_pairs, int num_blocks) {

@@ -4,7 +4,7 @@
 // K1 decode_f32_kernel    the same step in fp32 on the CUDA cores (exact-precision path)
 // K2 lse_reduce_kernel    merges split-context partitions with a log-sum-exp reduce
 // K3 kv_append_kernel     slot-mapped write of new tokens' K/V
-// K4 copy_blocks_kernel   whole-block copy for copy-on-write
+// K4 move_blocks_kernel   whole-block copies: copy-on-write, swap to/from a host pool, several layers
 // K5 validate_*_kernel    device-side range checks of the metadata
 //
 // The method ("PagedAttention: gestionar la KV cache como memoria de un
@@ -992,21 +992,82 @@ __global__ void kv_append_kernel(const uint4 *__restrict__ k, const uint4 *__res
 }
 
 // =====================================================================================
-// K4: block copy. grid (chunks, pairs, 2 caches); 16-byte vectors.
+// K4: whole-block moves. For each (src, dst) pair, block src of a source pool
+// is copied onto block dst of a destination pool -- every kv head, all 16
+// slots -- for each of `ncache` caches (K and V of one or more layers). The
+// pools are the same for copy-on-write, different for swapping to and from a
+// host pool (pinned host memory the GPU addresses directly) or between device
+// pools. grid (chunks, pairs, caches); 16-byte vectors.
 // =====================================================================================
-__global__ void copy_blocks_kernel(uint4 *__restrict__ kc, uint4 *__restrict__ vc, const int64_t *__restrict__ pairs,
-                                   int num_blocks, int64_t vec_per_block) {
-    const int pr = blockIdx.y;
+struct BlockMove {
+    const uint4 *src[2];                // K and V of one layer, given inline ...
+    uint4 *dst[2];
+    const uint4 *const *src_k_layers;   // ... or per-layer pointer arrays [layers]
+    const uint4 *const *src_v_layers;
+    uint4 *const *dst_k_layers;
+    uint4 *const *dst_v_layers;
+    int src_num_blocks, dst_num_blocks;
+    int64_t vec_per_block;
+};
+
+__global__ void move_blocks_kernel(const BlockMove m, const int64_t *__restrict__ pairs) {
+    const int pr = blockIdx.y, c = blockIdx.z;
     const int64_t src = __ldg(pairs + 2 * pr), dst = __ldg(pairs + 2 * pr + 1);
-    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0) raise_error(PKV_DEVERR_PAIR);
+    const bool lead = threadIdx.x == 0 && blockIdx.x == 0;
+    if (src < 0 || src >= m.src_num_blocks || dst < 0 || dst >= m.dst_num_blocks) {
+        if (lead && c == 0) raise_error(PKV_DEVERR_PAIR);
         return;
     }
-    uint4 *c = blockIdx.z ? vc : kc;
-    const uint4 *sp = c + src * vec_per_block;
-    uint4 *dp = c + dst * vec_per_block;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < vec_per_block; i += (int64_t)gridDim.x * blockDim.x)
+    const uint4 *sb;
+    uint4 *db;
+    if (m.src_k_layers) {
+        const int layer = c >> 1;
+        sb = (c & 1) ? m.src_v_layers[layer] : m.src_k_layers[layer];
+        db = (c & 1) ? m.dst_v_layers[layer] : m.dst_k_layers[layer];
+        if (((reinterpret_cast<uintptr_t>(sb) | reinterpret_cast<uintptr_t>(db)) & 15) != 0 || !sb || !db) {
+            if (lead && pr == 0) raise_error(PKV_DEVERR_POINTER);
+            return;
+        }
+    } else {
+        sb = m.src[c];
+        db = m.dst[c];
+    }
+    const uint4 *sp = sb + src * m.vec_per_block;
+    uint4 *dp = db + dst * m.vec_per_block;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < m.vec_per_block;
+         i += (int64_t)gridDim.x * blockDim.x)
         dp[i] = sp[i];
+}
+
+// K3 for several layers at once: grid (vector chunks, layers); layer l reads
+// k[l], v[l] ([T][Hkv][D]) and writes k_caches[l], v_caches[l] at the same slots.
+__global__ void kv_append_layers_kernel(const uint4 *const *k, const uint4 *const *v, const int64_t *__restrict__ slots,
+                                        uint4 *const *kc, uint4 *const *vc, int num_tokens, int num_kv_heads,
+                                        int vec_per_row, int num_blocks) {
+    const int layer = blockIdx.y;
+    const uint4 *kl = k[layer], *vl = v[layer];
+    uint4 *kcl = kc[layer], *vcl = vc[layer];
+    const bool lead = threadIdx.x == 0 && blockIdx.x == 0;
+    if (((reinterpret_cast<uintptr_t>(kl) | reinterpret_cast<uintptr_t>(vl) | reinterpret_cast<uintptr_t>(kcl) |
+          reinterpret_cast<uintptr_t>(vcl)) & 15) != 0 || !kl || !vl || !kcl || !vcl) {
+        if (lead) raise_error(PKV_DEVERR_POINTER);
+        return;
+    }
+    const int per_token = num_kv_heads * vec_per_row;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)num_tokens * per_token) return;
+    const int t = (int)(idx / per_token);
+    const int rem = (int)(idx - (long long)t * per_token);
+    const int64_t slot = __ldg(slots + t);
+    if (slot < 0) return;
+    if (slot >= (int64_t)num_blocks * kBlock) {
+        if (rem == 0 && layer == 0) raise_error(PKV_DEVERR_SLOT);
+        return;
+    }
+    const int hh = rem / vec_per_row, cc = rem - hh * vec_per_row;
+    const size_t dst = ((((size_t)(slot >> 4)) * num_kv_heads + hh) * kBlock + (slot & 15)) * vec_per_row + cc;
+    kcl[dst] = kl[idx];
+    vcl[dst] = vl[idx];
 }
 
 // =====================================================================================

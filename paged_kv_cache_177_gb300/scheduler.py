@@ -83,7 +83,13 @@ class Request:
 
 @dataclass
 class StepBatch:
-    """Device-call metadata of one decode step."""
+    """Device-call metadata of one decode step. The device runs it in this
+    order: swap-in copies (host pool -> device), prefill of newly admitted
+    sequences, swap-out copies (device -> host pool), copy-on-write copies,
+    the KV append of one token per running sequence, then attention over the
+    tables. (A sequence swapped in can be preempted again in the same step,
+    and blocks a swap-out releases can be written by the copies and appends
+    that follow, so no other order is safe.)"""
     seq_ids: List[int]
     cow_pairs: np.ndarray        # int64 [n, 2]
     slot_mapping: np.ndarray     # int64 [len(seq_ids)], one appended token per running sequence
@@ -91,41 +97,62 @@ class StepBatch:
     context_lens: np.ndarray     # int32 [len(seq_ids)]
     finished: List[int] = field(default_factory=list)
     preempted: List[int] = field(default_factory=list)
+    swap_out_pairs: np.ndarray = field(default_factory=lambda: np.zeros((0, 2), dtype=np.int64))  # (device, host)
+    swap_in_pairs: np.ndarray = field(default_factory=lambda: np.zeros((0, 2), dtype=np.int64))   # (host, device)
+    prefilled: List[Tuple[int, int, List[int]]] = field(default_factory=list)  # (sequence, tokens, its blocks)
 
 
 class IterationScheduler:
     """Continuous batching over a paged KV pool.
 
-    Each ``step()``: admit queued requests while a slot is free and the pool
-    holds their prompt blocks; reserve one slot per running sequence (taking
-    a new block only when the last is full, copying a shared partly filled
-    block first); if the pool runs dry, preempt the most recently admitted
-    sequence (free its blocks, put it back at the head of the queue to be
-    recomputed); then retire the sequences that reached their output length.
+    Each ``step()``: bring swapped-out sequences back first, then admit queued
+    requests while a slot is free and the pool holds their prompt blocks;
+    reserve one slot per running sequence (taking a new block only when the
+    last is full, copying a shared partly filled block first); if the pool
+    runs dry, preempt the most recently admitted sequence -- swap its blocks
+    out to the host pool when one is configured and has room, otherwise free
+    them and put the request back at the head of the queue to be recomputed;
+    then retire the sequences that reached their output length.
     """
 
     def __init__(self, num_blocks: int, max_batch: int, block_size: int = 16,
-                 order: Optional[np.ndarray] = None):
+                 order: Optional[np.ndarray] = None, host_blocks: int = 0):
         self.bm = BlockManager(num_blocks, block_size, order)
+        self.host = BlockManager(host_blocks, block_size) if host_blocks else None
         self.max_batch = int(max_batch)
         self.waiting: Deque[Request] = deque()
+        self.swapped: Deque[Request] = deque()
         self.running: List[Request] = []
         self.requests: Dict[int, Request] = {}
         self.steps = 0
         self.busy_slot_steps = 0
         self.preemptions = 0
+        self.swaps = 0
+        self._swap_out: List[Tuple[int, int]] = []
+        self._swap_in: List[Tuple[int, int]] = []
+        self._prefilled: List[Tuple[int, int, List[int]]] = []
 
     def add(self, req: Request) -> None:
         self.requests[req.req_id] = req
         self.waiting.append(req)
 
     def idle(self) -> bool:
-        return not self.waiting and not self.running
+        return not self.waiting and not self.running and not self.swapped
 
     def _admit(self) -> None:
+        while self.swapped and len(self.running) < self.max_batch:
+            req = self.swapped[0]
+            if not self.bm.can_allocate(len(self.host.block_table(req.req_id))):
+                return                      # swapped sequences go back before anything new
+            self._swap_in += self.bm.swap_in(req.req_id, self.host)
+            self.swapped.popleft()
+            self.running.append(req)
         while self.waiting and len(self.running) < self.max_batch:
             req = self.waiting[0]
-            if req.parent is not None and self.bm.has_seq(req.parent):
+            parent = self.requests.get(req.parent) if req.parent is not None else None
+            if (parent is not None and req.generated == 0 and parent.generated == 0
+                    and self.bm.has_seq(req.parent)):
+                # a fresh sample shares its parent's just-written prompt
                 self.bm.fork(req.parent, req.req_id)
             else:
                 # prefill writes the prompt (and anything generated before a preemption)
@@ -133,17 +160,26 @@ class IterationScheduler:
                 if not self.bm.can_allocate(need):
                     break
                 self.bm.allocate(req.req_id, req.prompt_len + req.generated)
+                self._prefilled.append((req.req_id, req.prompt_len + req.generated,
+                                        self.bm.block_table(req.req_id)))
             self.waiting.popleft()
             self.running.append(req)
 
     def _preempt_one(self) -> Request:
         victim = self.running.pop()
-        self.bm.free(victim.req_id)
-        self.waiting.appendleft(victim)
+        n = len(self.bm.block_table(victim.req_id))
+        if self.host is not None and self.host.can_allocate(n):
+            self._swap_out += self.bm.swap_out(victim.req_id, self.host)
+            self.swapped.appendleft(victim)
+            self.swaps += 1
+        else:
+            self.bm.free(victim.req_id)
+            self.waiting.appendleft(victim)
         self.preemptions += 1
         return victim
 
     def step(self) -> Optional[StepBatch]:
+        self._swap_out, self._swap_in, self._prefilled = [], [], []
         self._admit()
         if not self.running:
             return None
@@ -178,8 +214,9 @@ class IterationScheduler:
             req.generated += 1
             if req.generated >= req.output_len:
                 finished.append(req.req_id)
-        return StepBatch(ids, np.array(pairs, dtype=np.int64).reshape(-1, 2), np.array(slots, dtype=np.int64),
-                         tables, lens, finished, preempted)
+        as_pairs = lambda x: np.array(x, dtype=np.int64).reshape(-1, 2)
+        return StepBatch(ids, as_pairs(pairs), np.array(slots, dtype=np.int64), tables, lens, finished, preempted,
+                         as_pairs(self._swap_out), as_pairs(self._swap_in), list(self._prefilled))
 
     def retire(self, batch: StepBatch) -> None:
         """Free the blocks of the sequences the step finished."""
