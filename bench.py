@@ -489,7 +489,9 @@ def run_op(args, rank, world, local, dist):
       fresh device blocks) of the blocks of a quarter of the workload's
       sequences, as preemption does; GB/s of block bytes moved each way.
     --op append_layers: kv_append of one token per sequence into every layer's
-      caches (40 layers) in one launch, against one launch per layer."""
+      caches (40 layers) in one launch, against one launch per layer.
+    --op shared_prefix: shared-prefix decode on a workload with shared
+      prompts, against plain decode of the same batch."""
     from paged_kv_cache_177_gb300 import build
     build.build_library()
     from paged_kv_cache_177_gb300 import binding as B
@@ -526,7 +528,39 @@ def run_op(args, rank, world, local, dist):
         t = sorted(a.elapsed_time(b) for a, b in evs)
         return t[len(t) // 2] / 1e3
 
-    if args.op == "swap":
+    if args.op == "shared_prefix":
+        H = sp.num_q_heads
+        groups = torch.from_numpy(lay.group_members).to(dev)
+        shared = torch.from_numpy(lay.shared_blocks).to(dev)
+        if groups.shape[0] == 0:
+            raise SystemExit("--op shared_prefix needs a workload with shared prompts (parallel_sampling)")
+        out_c, out_p = torch.empty_like(w.q), torch.empty_like(w.q)
+        maxlen = lay.max_context_len
+        ws_c = torch.empty(B.shared_prefix_workspace_bytes(sp.num_seqs, H, sp.head_dim, maxlen, groups.shape[1]),
+                           dtype=torch.uint8, device=dev)
+        ws_p = torch.zeros(max(16, B.workspace_bytes(sp.num_seqs, H, sp.num_kv_heads, sp.head_dim, maxlen)),
+                           dtype=torch.uint8, device=dev)
+        B.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
+        B.copy_blocks(w.k_cache, w.v_cache, w.cow_pairs, host_pairs=lay.cow_pairs)
+        t_c = time_it(lambda: B.paged_decode_attention_shared_prefix(
+            out_c, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, groups, shared,
+            max_context_len=maxlen, workspace=ws_c), args.steps or 50)
+        t_p = time_it(lambda: B.paged_decode_attention(
+            out_p, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, max_context_len=maxlen,
+            workspace=ws_p), args.steps or 50)
+        logical, unique = lay.kv_bytes(eb), lay.unique_kv_bytes(eb)
+        peak, kind = peaks()
+        line = {"metric": "shared-prefix decode attention, logical KV GB/s", "unit": "GB/s",
+                "value": round(logical / t_c / 1e9, 2),
+                "shared_prefix": {"us": round(t_c * 1e6, 2), "logical_GB/s": round(logical / t_c / 1e9, 2),
+                                  "unique_GB/s": round(unique / t_c / 1e9, 2),
+                                  "unique_frac_of_peak": round(unique / t_c / 1e9 / peak, 4)},
+                "plain_decode": {"us": round(t_p * 1e6, 2), "logical_GB/s": round(logical / t_p / 1e9, 2)},
+                "speedup": round(t_p / t_c, 3), "logical_bytes": int(logical), "unique_bytes": int(unique),
+                "peak": peak, "peak_kind": kind, "higher_is_better": True,
+                "config": {"workload": describe(sp), "groups": int(groups.shape[0]),
+                           "shared_blocks": int(lay.shared_blocks[0])}}
+    elif args.op == "swap":
         seqs = np.arange(0, sp.num_seqs, 4)
         nblk = (lay.context_lens.astype(np.int64) + 15) // 16
         blocks = np.concatenate([lay.block_tables[s, :nblk[s]] for s in seqs]).astype(np.int64)
@@ -588,7 +622,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["step", "swap", "append_layers"], default="step",
+    ap.add_argument("--op", choices=["step", "swap", "append_layers", "shared_prefix"], default="step",
                     help="step: the decode step (the benchmark line); swap / append_layers: secondary measurements")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -145,6 +145,44 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
                            int partition_tokens, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * paged_decode_attention for a batch whose sequences share leading blocks --
+ * parallel samples of one prompt, a common system prompt ("Batching Continuo
+ * y PagedAttention", cruxr.ai, copy-on-write paragraph: the tables of requests
+ * with a common prefix point at the same physical blocks; "PagedAttention:
+ * gestionar la KV cache como memoria de un sistema operativo", section "El
+ * regalo extra: compartir memoria"). Results are those of
+ * paged_decode_attention on the same tables; the shared blocks are read from
+ * HBM once per group instead of once per sequence: a group's unit attends the
+ * union of its members' blocks -- the shared ones once for every member's
+ * query heads, each member's own blocks for that member's heads only.
+ *
+ * group_members: int32 [num_groups][group_size], sequence ids (-1 = empty
+ *   slot). The groups partition the batch: every sequence is listed exactly
+ *   once, a sequence that shares nothing as a group of one (a sequence not
+ *   listed gets no output).
+ * shared_blocks: int32 [num_groups]: leading blocks all members' tables hold
+ *   in common (same physical ids). The kernel uses at most the full blocks of
+ *   the group's shortest member and reads them through the first member's
+ *   table; the caller guarantees the members agree on them.
+ * group_size x (num_q_heads / num_kv_heads) must be at most 16. bf16 only.
+ * Partitions of partition_tokens split each group's union of blocks.
+ * workspace: at least pkv_shared_prefix_workspace_bytes(...) bytes (no
+ *   zero-fill needed). partition_tokens as for paged_decode_attention (> 0 or
+ *   0 for 512). Two launches: the prefix/suffix kernel and a merge kernel.
+ */
+int paged_decode_attention_shared_prefix(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                         const int32_t *block_tables, const int32_t *context_lens, float scale,
+                                         int num_kv_heads, int num_seqs, int num_q_heads, int head_dim,
+                                         int max_blocks_per_seq, int num_blocks, int max_context_len,
+                                         const int32_t *group_members, const int32_t *shared_blocks, int num_groups,
+                                         int group_size, pkv_dtype dtype, int partition_tokens, void *workspace,
+                                         size_t workspace_bytes, void *stream);
+
+/* Workspace bytes paged_decode_attention_shared_prefix needs. */
+size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
+                                         int group_size, int partition_tokens);
+
+/*
  * KV append: for each token t with slot = slot_mapping[t] >= 0,
  *   k_cache[slot / 16][h][slot % 16][:] = k[t][h][:]   (and v) for every kv head h.
  * Negative slots are skipped (padding). Slots >= num_blocks*16 are skipped

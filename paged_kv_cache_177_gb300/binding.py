@@ -46,6 +46,9 @@ _workspace_bytes = _decl("pkv_decode_workspace_bytes", _sz, _i, _i, _i, _i, _i, 
 _decode_launches = _decl("pkv_decode_launches", _i, _i, _i, _i, _i, _i)
 _decode = _decl("paged_decode_attention", _i, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                 _vp, _sz, _vp)
+_shared = _decl("paged_decode_attention_shared_prefix", _i, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i,
+                _i, _i, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp)
+_shared_ws = _decl("pkv_shared_prefix_workspace_bytes", _sz, _i, _i, _i, _i, _i, _i)
 _append = _decl("kv_append", _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
 _copy = _decl("copy_blocks", _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
 _swap = _decl("swap_blocks", _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp)
@@ -182,6 +185,62 @@ def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
     decode_raw(decode_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
                            max_context_len=max_context_len, partition_tokens=partition_tokens, workspace=workspace,
                            stream=stream))
+    return out
+
+
+def shared_prefix_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int, max_context_len: int,
+                                  group_size: int, partition_tokens: int = 0) -> int:
+    return int(_shared_ws(num_seqs, num_q_heads, head_dim, max_context_len, group_size, partition_tokens))
+
+
+def prefix_groups(num_seqs: int, groups, shared_blocks):
+    """Completes a partial grouping into the partition the shared-prefix call
+    takes: ``groups`` lists the sharing groups (sequence ids per group), every
+    sequence not in one becomes a group of one with no shared blocks.
+    Returns (group_members int32 [G, M] with -1 padding, shared_blocks int32 [G])."""
+    groups = [list(map(int, g)) for g in groups]
+    seen = {s for g in groups for s in g}
+    if len(seen) != sum(len(g) for g in groups):
+        raise ValueError("a sequence is in two groups")
+    groups += [[s] for s in range(num_seqs) if s not in seen]
+    shared = list(map(int, shared_blocks)) + [0] * (len(groups) - len(shared_blocks))
+    width = max([len(g) for g in groups] + [1])
+    members = np.full((len(groups), width), -1, dtype=np.int32)
+    for i, g in enumerate(groups):
+        members[i, :len(g)] = g
+    return members, np.array(shared, dtype=np.int32)
+
+
+def paged_decode_attention_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                         v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                         context_lens: torch.Tensor, scale: float, group_members: torch.Tensor,
+                                         shared_blocks: torch.Tensor, *, max_context_len: Optional[int] = None,
+                                         partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                                         stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """paged_decode_attention with the leading blocks shared by each group of
+    sequences read once per group.  group_members: int32 [G, M] sequence ids
+    (-1 = empty slot), listing every sequence exactly once (see
+    ``prefix_groups``); shared_blocks: int32 [G] blocks the members share."""
+    dev = _dev(out, q, k_cache, v_cache, block_tables, context_lens, group_members, shared_blocks)
+    if q.dtype != torch.bfloat16 or not (out.dtype == k_cache.dtype == v_cache.dtype == q.dtype):
+        raise TypeError("shared-prefix decode is bf16")
+    if group_members.dtype != torch.int32 or shared_blocks.dtype != torch.int32 or group_members.dim() != 2:
+        raise TypeError("group_members int32 [G, M] and shared_blocks int32 [G]")
+    G, M = group_members.shape
+    if shared_blocks.shape != (G,):
+        raise ValueError("shared_blocks must be [G]")
+    S, Hq, D = q.shape
+    NB, Hkv, P, _ = k_cache.shape
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    need = shared_prefix_workspace_bytes(S, Hq, D, max_context_len, max(M, 1), partition_tokens)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_shared(_p(out), _p(q), _p(k_cache), _p(v_cache), _p(block_tables), _p(context_lens), float(scale), Hkv, S,
+                   Hq, D, block_tables.shape[1], NB, int(max_context_len), _p(group_members) if G else None,
+                   _p(shared_blocks) if G else None, G, max(M, 1), PKV_BF16, int(partition_tokens), _p(workspace),
+                   ws_bytes, _stream_ptr(dev, stream)), "paged_decode_attention_shared_prefix")
     return out
 
 

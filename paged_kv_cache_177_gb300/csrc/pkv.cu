@@ -123,6 +123,25 @@ int launch_f32(const pkv::DecodeParams &p, dim3 grid, cudaStream_t st) {
     return check_launch();
 }
 
+template <int D, int NT>
+int launch_cascade(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, dim3 grid,
+                   cudaStream_t st) {
+    using C = pkv::Bf16Cfg<D, NT, kNstage, kNcw>;
+    auto kern = pkv::decode_bf16_cascade_kernel<D, NT, kNstage, kNcw>;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (configured_device != dev) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured_device = dev;
+    }
+    kern<<<grid, C::kThreads, C::kSmem, st>>>(tmk, tmv, p);
+    if (check_launch() != PKV_OK) return PKV_ERR_CUDA;
+    pkv::cascade_reduce_kernel<D><<<dim3(p.num_q_heads, p.group_size, p.num_groups), D, 0, st>>>(p);
+    return check_launch();
+}
+
 template <int D>
 int launch_reduce(const pkv::DecodeParams &p, pkv_dtype dt, cudaStream_t st) {
     constexpr int PG = 512 / D;  // partition groups: 512 threads per row
@@ -167,11 +186,11 @@ int sm_count(int *n) {
     return PKV_OK;
 }
 
-template <int D, int NT, int NS>
+template <int D, int NT, int NS, int NW>
 int launch_persistent(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, cudaStream_t st) {
-    using C = pkv::PersistCfg<D, NT, NS, kPersistWarps>;
+    using C = pkv::PersistCfg<D, NT, NS, NW>;
     static_assert(C::smem_bytes(kPersistMaxSeqs) + 64 <= kSmemLimit, "persistent kernel exceeds shared memory");
-    auto kern = pkv::decode_bf16_persistent_kernel<D, NT, NS, kPersistWarps>;
+    auto kern = pkv::decode_bf16_persistent_kernel<D, NT, NS, NW>;
     static thread_local int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -376,6 +395,90 @@ int pkv_check_swap_pairs(const int64_t *host_pairs, int num_pairs, int src_num_b
     return PKV_OK;
 }
 
+// Partitions of one union unit: at most group_size contexts' blocks.
+int cascade_parts(int group_size, int max_context_len, int pt) {
+    const long long blocks = (long long)group_size * ((max_context_len + 15) / 16);
+    return (int)((blocks * 16 + pt - 1) / pt);
+}
+
+size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
+                                         int group_size, int partition_tokens) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 || partition_tokens < 0 ||
+        group_size <= 0)
+        return 0;
+    const int pt = pkv_decode_partition_tokens(num_seqs, 1, max_context_len, partition_tokens);
+    if (pt % 16 != 0) return 0;
+    const int parts = cascade_parts(group_size, max_context_len, pt);
+    return (size_t)num_seqs * num_q_heads * (size_t)(parts > 0 ? parts : 1) * (2 + (size_t)head_dim) * sizeof(float);
+}
+
+int paged_decode_attention_shared_prefix(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                         const int32_t *block_tables, const int32_t *context_lens, float scale,
+                                         int num_kv_heads, int num_seqs, int num_q_heads, int head_dim,
+                                         int max_blocks_per_seq, int num_blocks, int max_context_len,
+                                         const int32_t *group_members, const int32_t *shared_blocks, int num_groups,
+                                         int group_size, pkv_dtype dtype, int partition_tokens, void *workspace,
+                                         size_t workspace_bytes, void *stream) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+        max_context_len < 0 || partition_tokens < 0 || num_groups < 0 || group_size <= 0)
+        return PKV_ERR_ARG;
+    if (dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0) return PKV_ERR_ARG;
+    const int g = num_q_heads / num_kv_heads;
+    if (g * group_size > 16 || group_size > 16) return PKV_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return PKV_ERR_ARG;
+    if (num_seqs > 65535 || num_kv_heads > 65535 || num_groups > 65535) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)num_blocks * num_kv_heads * 16 >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_ARG;
+    if (num_groups > 0 && (!group_members || !shared_blocks)) return PKV_ERR_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+    const int pt = pkv_decode_partition_tokens(num_seqs, num_kv_heads, max_context_len, partition_tokens);
+    if (pt % 16 != 0) return PKV_ERR_ARG;
+    const int parts = cascade_parts(group_size, max_context_len, pt);
+    if (parts > kMaxParts) return PKV_ERR_UNSUPPORTED;
+    const size_t need = pkv_shared_prefix_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
+                                                          group_size, partition_tokens);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
+
+    pkv::DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = g;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.max_context_len = max_context_len;
+    p.part_blocks = pt / 16;
+    p.max_parts = parts > 0 ? parts : 1;
+    p.pre_parts = 0;
+    p.ws_ml = static_cast<float *>(workspace);
+    p.ws_o = static_cast<float *>(workspace) + (size_t)num_seqs * num_q_heads * p.max_parts * 2;
+    p.group_members = group_members;
+    p.shared_blocks = shared_blocks;
+    p.num_groups = num_groups;
+    p.group_size = group_size;
+    alignas(64) CUtensorMap tmk, tmv;
+    int rc;
+    if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
+    if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
+    if (num_groups == 0) return PKV_OK;
+    const dim3 grid(p.max_parts, num_kv_heads, num_groups);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool wide = g * group_size > 8;
+    if (head_dim == 128)
+        return wide ? launch_cascade<128, 2>(tmk, tmv, p, grid, st) : launch_cascade<128, 1>(tmk, tmv, p, grid, st);
+    return wide ? launch_cascade<64, 2>(tmk, tmv, p, grid, st) : launch_cascade<64, 1>(tmk, tmv, p, grid, st);
+}
+
 int pkv_check_copy_pairs(const int64_t *host_pairs, int num_pairs, int num_blocks) {
     if (num_pairs < 0 || num_blocks <= 0) return PKV_ERR_ARG;
     if (num_pairs > 0 && !host_pairs) return PKV_ERR_ARG;
@@ -487,11 +590,14 @@ int decode_dispatch(void *out, const void *q, const void *k_cache, const void *v
         int rc;
         if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
         if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
-        constexpr int ns128 = PKV_PERSIST_STAGES_D128, ns64 = PKV_PERSIST_STAGES_D64;
+        // groups wider than 8 need two MMA column tiles: half the warps, twice the stages,
+        // so their registers fit without spilling
+        constexpr int ns128 = PKV_PERSIST_STAGES_D128, ns64 = PKV_PERSIST_STAGES_D64, nw = kPersistWarps;
         if (head_dim == 128)
-            return g <= 8 ? launch_persistent<128, 1, ns128>(tmk, tmv, p, st)
-                          : launch_persistent<128, 2, ns128>(tmk, tmv, p, st);
-        return g <= 8 ? launch_persistent<64, 1, ns64>(tmk, tmv, p, st) : launch_persistent<64, 2, ns64>(tmk, tmv, p, st);
+            return g <= 8 ? launch_persistent<128, 1, ns128, nw>(tmk, tmv, p, st)
+                          : launch_persistent<128, 2, 2 * ns128, nw / 2>(tmk, tmv, p, st);
+        return g <= 8 ? launch_persistent<64, 1, ns64, nw>(tmk, tmv, p, st)
+                      : launch_persistent<64, 2, 2 * ns64, nw / 2>(tmk, tmv, p, st);
     }
 
     const size_t grid_ws = grid_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, pt);

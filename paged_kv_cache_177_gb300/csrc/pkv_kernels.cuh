@@ -19,6 +19,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <climits>
+
 #include "pagedkv.h"
 #include "pkv_ptx.cuh"
 
@@ -47,7 +49,13 @@ struct DecodeParams {
     int max_parts;                // partitions allotted per (sequence, head) in the workspace
     int *counters;                // persistent kernel: [S][Hkv] arrival counters, zero between calls
     float *partials;              // persistent kernel: [workers][2][g][2 + D] segment states
+    // shared-prefix (cascade) decode
+    const int32_t *group_members; // [num_groups][group_size] sequence ids, -1 = empty
+    const int32_t *shared_blocks; // [num_groups] leading blocks the members share
+    int num_groups, group_size;
+    int pre_parts;                // workspace slots per row reserved for the prefix parts
 };
+
 
 // A sequence's usable length: negative lengths and lengths past the table or
 // past max_context_len are clamped (and flagged by thread 0 of one CTA).
@@ -60,6 +68,24 @@ __device__ __forceinline__ int seq_len(const DecodeParams &p, int s, bool flag) 
     }
     return len;
 }
+
+// Sum or max over the CTA (all threads call it; scratch holds 32 floats).
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float *scratch) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = is_max ? fmaxf(v, w) : v + w;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    v = is_max ? -INFINITY : 0.f;
+    for (int w = 0; w < nw; ++w) v = is_max ? fmaxf(v, scratch[w]) : v + scratch[w];
+    return v;
+}
+
+
 
 // =====================================================================================
 // The per-block step shared by both bf16 decode kernels. One warp attends a
@@ -115,15 +141,36 @@ struct WarpAttn {
         load_q_frags(qf, q_group, g, lane);
     }
 
+    // Columns gathered from any query rows: row_of(column) is the row index
+    // into q ([rows][D]) of MMA column `column`, or -1 for an unused column.
+    template <class RowOf>
+    __device__ __forceinline__ void load_q_rows(const __nv_bfloat16 *q, RowOf row_of, int lane) {
+        const int gq = lane >> 2, t4 = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int row = row_of(nt * 8 + gq);
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(q + (size_t)(row >= 0 ? row : 0) * D);
+#pragma unroll
+            for (int kk = 0; kk < kSteps; ++kk) {
+                qf[kk][nt][0] = row >= 0 ? __ldg(qrow + (16 * kk + 2 * t4) / 2) : 0u;
+                qf[kk][nt][1] = row >= 0 ? __ldg(qrow + (16 * kk + 8 + 2 * t4) / 2) : 0u;
+            }
+        }
+    }
+
     // Attends one staged tile: sk, sv = shared addresses of the K and V tiles.
     // Rows below `lo` are not tokens of the sequence: the last block of a
     // sequence with v valid tokens is loaded shifted down by lo = 16 - v rows,
     // so its first lo rows arrive zero-filled (zero V rows cannot poison the
     // product) and are masked out of the softmax here.
-    __device__ __forceinline__ void block(uint32_t sk, uint32_t sv, int lo, float scale_log2, int lane) {
+    // col_lo, col_hi: the MMA columns this block is attended for (columns
+    // outside get no weight from it; a shared-prefix unit attends each
+    // member's own blocks for that member's columns only).
+    __device__ __forceinline__ void block(uint32_t sk, uint32_t sv, int lo, float scale_log2, int lane,
+                                          int col_lo = 0, int col_hi = 8 * NT) {
         float sc[NT][4];
         scores(sk, sc, lane);
-        softmax_pv(sc, sv, lo, scale_log2, lane);
+        softmax_pv(sc, sv, lo, scale_log2, lane, col_lo, col_hi);
     }
 
     // S^T = K . Q^T for the 16 tokens of the staged K tile (two independent
@@ -159,17 +206,19 @@ struct WarpAttn {
     // Online-softmax update with the block's scores, then O^T += V^T . P^T
     // from the staged V tile.
     __device__ __forceinline__ void softmax_pv(const float (&sc)[NT][4], uint32_t sv, int lo, float scale_log2,
-                                               int lane) {
-        const int gq = lane >> 2;
+                                               int lane, int col_lo = 0, int col_hi = 8 * NT) {
+        const int gq = lane >> 2, t4 = lane & 3;
         const int mi = lane >> 3, r8 = lane & 7;
         const bool v0 = gq >= lo, v1 = gq + 8 >= lo;
         uint32_t pb0[NT], pb1[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const float x0 = v0 ? sc[nt][0] * scale_log2 : -INFINITY;
-            const float x1 = v0 ? sc[nt][1] * scale_log2 : -INFINITY;
-            const float x2 = v1 ? sc[nt][2] * scale_log2 : -INFINITY;
-            const float x3 = v1 ? sc[nt][3] * scale_log2 : -INFINITY;
+            const int c0 = nt * 8 + 2 * t4;
+            const bool k0 = c0 >= col_lo && c0 < col_hi, k1 = c0 + 1 >= col_lo && c0 + 1 < col_hi;
+            const float x0 = (v0 && k0) ? sc[nt][0] * scale_log2 : -INFINITY;
+            const float x1 = (v0 && k1) ? sc[nt][1] * scale_log2 : -INFINITY;
+            const float x2 = (v1 && k0) ? sc[nt][2] * scale_log2 : -INFINITY;
+            const float x3 = (v1 && k1) ? sc[nt][3] * scale_log2 : -INFINITY;
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) {
@@ -177,12 +226,14 @@ struct WarpAttn {
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
             }
             const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
-            const float al0 = ex2_approx(m[nt][0] - mn0), al1 = ex2_approx(m[nt][1] - mn1);
+            // a column that has seen no token yet keeps max -inf: exponentiate against 0
+            const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = ex2_approx(m[nt][0] - ms0), al1 = ex2_approx(m[nt][1] - ms1);
             m[nt][0] = mn0;
             m[nt][1] = mn1;
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(ex2_approx(x0 - mn0), ex2_approx(x1 - mn1));
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(ex2_approx(x2 - mn0), ex2_approx(x3 - mn1));
-            const float2 flo = __bfloat1622float2(lo), fhi = __bfloat1622float2(hi);
+            const __nv_bfloat162 plo = __floats2bfloat162_rn(ex2_approx(x0 - ms0), ex2_approx(x1 - ms1));
+            const __nv_bfloat162 phi = __floats2bfloat162_rn(ex2_approx(x2 - ms0), ex2_approx(x3 - ms1));
+            const float2 flo = __bfloat1622float2(plo), fhi = __bfloat1622float2(phi);
             // the sum uses the rounded weights the PV product uses, so they stay normalised
             l[nt][0] = l[nt][0] * al0 + (flo.x + fhi.x);
             l[nt][1] = l[nt][1] * al1 + (flo.y + fhi.y);
@@ -194,8 +245,8 @@ struct WarpAttn {
                 acc[mt][nt][3] *= al1;
             }
             // P^T as the B operand of PV: transpose the (token x head) 8x8 quads
-            pb0[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&lo));
-            pb1[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&hi));
+            pb0[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&plo));
+            pb1[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t *>(&phi));
         }
 
 #pragma unroll
@@ -252,6 +303,114 @@ struct Bf16Cfg {
     static_assert(NSTAGE % NCW == 0, "each stage is always consumed by the same warp");
 };
 
+// Producer warp of the grid kernels: stages blocks [b0, b0 + nb) of one
+// sequence's table row into the ring, 32 block ids at a time. `last_block` is
+// the index of the sequence's last block and `last_valid` its token count
+// (that block is loaded early so its slots past the end arrive zero-filled).
+template <class C, int NSTAGE>
+__device__ __forceinline__ void grid_produce(const CUtensorMap &tmk, const CUtensorMap &tmv, const int32_t *table_row,
+                                             int b0, int nb, int last_block, int last_valid, int num_blocks,
+                                             int num_kv_heads, int h, uint8_t *base, uint64_t *full, uint64_t *empty,
+                                             int lane) {
+    bool ok = true;
+    for (int jb = 0; jb < nb && ok; jb += 32) {
+        const int mine = (jb + lane < nb) ? __ldg(table_row + b0 + jb + lane) : 0;
+        const int cnt = min(32, nb - jb);
+        for (int i = 0; i < cnt; ++i) {
+            const int pb = __shfl_sync(0xffffffffu, mine, i);
+            const int j = jb + i;
+            if (lane == 0) {
+                const int st = j % NSTAGE;
+                if (j >= NSTAGE && !mbar_wait(&empty[st], ((j / NSTAGE) - 1) & 1)) {
+                    raise_error(PKV_DEVERR_TIMEOUT);
+                    ok = false;
+                }
+                if (ok) {
+                    int z;
+                    if (pb < 0 || pb >= num_blocks) {
+                        raise_error(PKV_DEVERR_BLOCK_ID);
+                        z = -1;  // outside the tensor: the tile reads as zeros
+                    } else {
+                        z = pb * num_kv_heads + h;
+                    }
+                    const int y = (b0 + j == last_block) ? last_valid - kBlock : 0;
+                    mbar_arrive_expect_tx(&full[st], C::kStage);
+                    uint8_t *sk = base + st * C::kStage;
+                    tma_load_4d(sk, &tmk, 0, y, 0, z, &full[st]);
+                    tma_load_4d(sk + C::kTile, &tmv, 0, y, 0, z, &full[st]);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+        }
+    }
+}
+
+// Consumer warps of the grid kernels: blocks j = warp, warp + NCW, ... of the
+// staged range (block_args(j, stage) gives each block's early-loaded rows and
+// column range), then the warps' states merged through shared memory. For
+// each column c < ncols (an MMA column: a query head of a query sequence)
+// and head-dim index d, emit(c, d, o, M, L) receives the column's output
+// o = O / L and its (max, sum) in the log2 domain.
+template <class C, int D, int NT, int NSTAGE, int NCW, class BlockArgs, class Emit>
+__device__ __forceinline__ void grid_consume(WarpAttn<D, NT> &wa, int nb, BlockArgs block_args, float scale_log2,
+                                             uint8_t *base, uint64_t *full, uint64_t *empty, int ncols, int warp,
+                                             int lane, int tid, Emit emit) {
+    const int gq = lane >> 2, t4 = lane & 3;
+    for (int j = warp; j < nb; j += NCW) {
+        const int st = j % NSTAGE;
+        if (!mbar_wait(&full[st], (j / NSTAGE) & 1)) {
+            raise_error(PKV_DEVERR_TIMEOUT);
+            break;
+        }
+        const uint32_t sk = smem_u32(base + st * C::kStage);
+        const int3 a = block_args(j, st);  // (rows loaded early, first column, column end)
+        wa.block(sk, sk + C::kTile, a.x, scale_log2, lane, a.y, a.z);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    wa.reduce_l();
+    named_barrier_sync(1, NCW * 32);  // every consumer is done with the stage ring
+    float *mml = reinterpret_cast<float *>(base);                    // [NCW][kHeads][2]
+    float *macc = mml + NCW * C::kHeads * 2;                         // [NCW][kHeads][kMergeStride]
+    if (gq == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int head = nt * 8 + 2 * t4 + c;
+                mml[(warp * C::kHeads + head) * 2 + 0] = wa.m[nt][c];
+                mml[(warp * C::kHeads + head) * 2 + 1] = wa.l[nt][c];
+            }
+    }
+#pragma unroll
+    for (int mt = 0; mt < C::kSteps; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int head = nt * 8 + 2 * t4 + (e & 1);
+                const int d = 16 * mt + gq + (e >> 1) * 8;
+                macc[(warp * C::kHeads + head) * C::kMergeStride + d] = wa.acc[mt][nt][e];
+            }
+    named_barrier_sync(1, NCW * 32);
+    for (int idx = tid; idx < ncols * D; idx += NCW * 32) {
+        const int col = idx / D, d = idx - col * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, mml[(w * C::kHeads + col) * 2]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+            const float mw = mml[(w * C::kHeads + col) * 2];
+            const float f = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
+            L += mml[(w * C::kHeads + col) * 2 + 1] * f;
+            O += macc[(w * C::kHeads + col) * C::kMergeStride + d] * f;
+        }
+        emit(col, d, O / L, M, L);
+    }
+}
+
 template <int D, int NT, int NSTAGE, int NCW>
 __global__ void __launch_bounds__((NCW + 1) * 32)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -295,115 +454,30 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
     __syncthreads();
 
     if (warp == NCW) {
-        // ------------------------------ producer ------------------------------
-        const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks_per_seq + b_begin;
-        bool ok = true;
-        for (int jb = 0; jb < nb && ok; jb += 32) {
-            const int mine = (jb + lane < nb) ? __ldg(bt + jb + lane) : 0;
-            const int cnt = min(32, nb - jb);
-            for (int i = 0; i < cnt; ++i) {
-                const int pb = __shfl_sync(0xffffffffu, mine, i);
-                const int j = jb + i;
-                if (lane == 0) {
-                    const int st = j % NSTAGE;
-                    if (j >= NSTAGE && !mbar_wait(&empty[st], ((j / NSTAGE) - 1) & 1)) {
-                        raise_error(PKV_DEVERR_TIMEOUT);
-                        ok = false;
-                    }
-                    if (ok) {
-                        int z;
-                        if (pb < 0 || pb >= p.num_blocks) {
-                            raise_error(PKV_DEVERR_BLOCK_ID);
-                            z = -1;  // outside the tensor: the tile reads as zeros
-                        } else {
-                            z = pb * p.num_kv_heads + h;
-                        }
-                        // the sequence's last block: start last_valid - 16 rows early (zero fill)
-                        const int y = (b_begin + j == nblk - 1) ? last_valid - kBlock : 0;
-                        mbar_arrive_expect_tx(&full[st], C::kStage);
-                        uint8_t *sk = base + st * C::kStage;
-                        tma_load_4d(sk, &tmk, 0, y, 0, z, &full[st]);
-                        tma_load_4d(sk + C::kTile, &tmv, 0, y, 0, z, &full[st]);
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-            }
-        }
+        grid_produce<C, NSTAGE>(tmk, tmv, p.block_tables + (size_t)s * p.max_blocks_per_seq, b_begin, nb, nblk - 1,
+                                last_valid, p.num_blocks, p.num_kv_heads, h, base, full, empty, lane);
         return;
     }
-
-    // ------------------------------ consumers ------------------------------
-    const int gq = lane >> 2, t4 = lane & 3;
     WarpAttn<D, NT> wa;
     wa.load_q(static_cast<const __nv_bfloat16 *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)h * g) * D, g, lane);
     wa.reset();
-    for (int j = warp; j < nb; j += NCW) {
-        const int st = j % NSTAGE;
-        if (!mbar_wait(&full[st], (j / NSTAGE) & 1)) {
-            raise_error(PKV_DEVERR_TIMEOUT);
-            break;
-        }
-        const uint32_t sk = smem_u32(base + st * C::kStage);
-        const int lo = (b_begin + j == nblk - 1) ? kBlock - last_valid : 0;
-        wa.block(sk, sk + C::kTile, lo, p.scale_log2, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-    }
-
-    // ---------------- merge the consumer warps' states ----------------
-    wa.reduce_l();
-    named_barrier_sync(1, NCW * 32);  // every consumer is done with the stage ring
-    float *mml = reinterpret_cast<float *>(base);                    // [NCW][kHeads][2]
-    float *macc = mml + NCW * C::kHeads * 2;                         // [NCW][kHeads][kMergeStride]
-    if (gq == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int head = nt * 8 + 2 * t4 + c;
-                mml[(warp * C::kHeads + head) * 2 + 0] = wa.m[nt][c];
-                mml[(warp * C::kHeads + head) * 2 + 1] = wa.l[nt][c];
+    const size_t orow0 = (size_t)s * p.num_q_heads + (size_t)h * g;
+    const int last_in_range = (b_begin + nb - 1 == nblk - 1) ? nb - 1 : -1;
+    grid_consume<C, D, NT, NSTAGE, NCW>(
+        wa, nb,
+        [&](int j, int) { return make_int3(j == last_in_range ? kBlock - last_valid : 0, 0, C::kHeads); },
+        p.scale_log2, base, full, empty, g, warp, lane, tid, [&](int col, int d, float o, float M, float L) {
+            if (npart == 1) {
+                out[(orow0 + col) * D + d] = __float2bfloat16_rn(o);
+            } else {
+                const size_t r = (orow0 + col) * p.max_parts + part;
+                p.ws_o[r * D + d] = o;
+                if (d == 0) {
+                    p.ws_ml[r * 2 + 0] = M;
+                    p.ws_ml[r * 2 + 1] = L;
+                }
             }
-    }
-#pragma unroll
-    for (int mt = 0; mt < C::kSteps; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int head = nt * 8 + 2 * t4 + (e & 1);
-                const int d = 16 * mt + gq + (e >> 1) * 8;
-                macc[(warp * C::kHeads + head) * C::kMergeStride + d] = wa.acc[mt][nt][e];
-            }
-    named_barrier_sync(1, NCW * 32);
-
-    for (int idx = tid; idx < g * D; idx += NCW * 32) {
-        const int head = idx / D, d = idx - head * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) M = fmaxf(M, mml[(w * C::kHeads + head) * 2]);
-        float L = 0.f, O = 0.f;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) {
-            const float mw = mml[(w * C::kHeads + head) * 2];
-            const float f = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
-            L += mml[(w * C::kHeads + head) * 2 + 1] * f;
-            O += macc[(w * C::kHeads + head) * C::kMergeStride + d] * f;
-        }
-        const float o = O / L;
-        const size_t orow = (size_t)s * p.num_q_heads + (size_t)h * g + head;
-        if (npart == 1) {
-            out[orow * D + d] = __float2bfloat16_rn(o);
-        } else {
-            const size_t r = orow * p.max_parts + part;
-            p.ws_o[r * D + d] = o;
-            if (d == 0) {
-                p.ws_ml[r * 2 + 0] = M;
-                p.ws_ml[r * 2 + 1] = L;
-            }
-        }
-    }
+        });
 }
 
 // =====================================================================================
@@ -791,6 +865,215 @@ __global__ void __launch_bounds__(NW * 32, 1)
 }
 
 // =====================================================================================
+// K1 (bf16, shared prefix): decode for batches whose sequences share leading
+// blocks -- parallel samples of one prompt, a common system prompt
+// ("Batching Continuo y PagedAttention", cruxr.ai, copy-on-write paragraph:
+// the tables of requests with a common prefix point at the same physical
+// blocks). A unit is a group and a kv head; its blocks are the union of the
+// members' contexts: the shared prefix once (read through the first member's
+// table), then each member's own blocks. All members' query heads are the
+// MMA columns (member m, head n = column m * g + n); a prefix block is
+// attended for every column, a member's own block for that member's columns
+// only, so each column's online softmax covers exactly its sequence's
+// context and each shared block is read from HBM once per group. Sequences in
+// no group are listed as groups of one. grid (partition, kv head, group).
+// Every partition leaves a (max, sum, output) state per column;
+// cascade_reduce_kernel merges a row's states with the log-sum-exp rule.
+// =====================================================================================
+constexpr int kMaxGroup = 16;
+
+struct UnionUnit {
+    int count;                   // members (valid ones, in slot order)
+    int prefix;                  // shared blocks, read through member 0's table
+    int total;                   // blocks in the union
+    int member[kMaxGroup];       // sequence ids
+    int len[kMaxGroup];          // their context lengths
+    int own[kMaxGroup + 1];      // union position where each member's own blocks start
+};
+
+// Builds group z's union unit in shared memory with one warp (lane m reads
+// member slot m): members in slot order, the blocks they share (cut to the
+// shortest member's full blocks), and where each member's own blocks start.
+__device__ __forceinline__ void union_unit(const DecodeParams &p, int z, UnionUnit &u, int lane, bool flag) {
+    const int M = p.group_size;
+    int sm = -1, len = 0;
+    if (lane < M) {
+        sm = __ldg(p.group_members + (size_t)z * M + lane);
+        if (sm < 0 || sm >= p.num_seqs) sm = -1;
+        else len = seq_len(p, sm, flag);
+    }
+    const unsigned valid = __ballot_sync(0xffffffffu, sm >= 0);
+    int pb = sm >= 0 ? len / kBlock : INT_MAX;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pb = min(pb, __shfl_xor_sync(0xffffffffu, pb, o));
+    const int shared = valid ? min(pb, max(__ldg(p.shared_blocks + z), 0)) : 0;
+    const int idx = __popc(valid & ((1u << lane) - 1));   // this member's place among the valid ones
+    const int own = sm >= 0 ? (len + kBlock - 1) / kBlock - shared : 0;
+    int incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (sm >= 0) {
+        u.member[idx] = sm;
+        u.len[idx] = len;
+        u.own[idx] = shared + incl - own;
+    }
+    if (lane == 31) {
+        u.count = __popc(valid);
+        u.prefix = shared;
+        u.total = shared + incl;
+        u.own[__popc(valid)] = shared + incl;
+    }
+}
+
+template <int D, int NT, int NSTAGE, int NCW>
+__global__ void __launch_bounds__((NCW + 1) * 32)
+    decode_bf16_cascade_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                               const DecodeParams p) {
+    using C = Bf16Cfg<D, NT, NSTAGE, NCW>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ UnionUnit u;
+    __shared__ int2 stage_info[NSTAGE];  // per stage: (member or -1 for the prefix, rows loaded early)
+
+    const int part = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = p.group;
+    if (warp == 0) union_unit(p, z, u, lane, part == 0 && h == 0);
+    __syncthreads();
+    const int j0 = part * p.part_blocks;
+    if (u.count == 0 || j0 >= u.total) return;
+    const int nb = min(u.total - j0, p.part_blocks);
+
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + C::kBarOffset);
+    uint64_t *empty = full + NSTAGE;
+    if (tid == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == NCW) {
+        // ------------------------------ producer ------------------------------
+        bool ok = true;
+        for (int jb = 0; jb < nb && ok; jb += 32) {
+            int pb = 0, mem = -1, early = 0;
+            if (jb + lane < nb) {
+                const int j = j0 + jb + lane;
+                int row = u.member[0], blk = j;
+                if (j >= u.prefix) {
+                    mem = 0;
+                    while (j >= u.own[mem + 1]) ++mem;
+                    row = u.member[mem];
+                    blk = u.prefix + (j - u.own[mem]);
+                    const int nblk = (u.len[mem] + kBlock - 1) / kBlock;
+                    if (blk == nblk - 1) early = kBlock * nblk - u.len[mem];
+                }
+                pb = __ldg(p.block_tables + (size_t)row * p.max_blocks_per_seq + blk);
+            }
+            const int cnt = min(32, nb - jb);
+            for (int i = 0; i < cnt; ++i) {
+                const int bpb = __shfl_sync(0xffffffffu, pb, i);
+                const int bmem = __shfl_sync(0xffffffffu, mem, i);
+                const int bearly = __shfl_sync(0xffffffffu, early, i);
+                const int jj = jb + i;
+                if (lane == 0) {
+                    const int st = jj % NSTAGE;
+                    if (jj >= NSTAGE && !mbar_wait(&empty[st], ((jj / NSTAGE) - 1) & 1)) {
+                        raise_error(PKV_DEVERR_TIMEOUT);
+                        ok = false;
+                    }
+                    if (ok) {
+                        int zt;
+                        if (bpb < 0 || bpb >= p.num_blocks) {
+                            raise_error(PKV_DEVERR_BLOCK_ID);
+                            zt = -1;
+                        } else {
+                            zt = bpb * p.num_kv_heads + h;
+                        }
+                        stage_info[st] = make_int2(bmem, bearly);
+                        mbar_arrive_expect_tx(&full[st], C::kStage);
+                        uint8_t *sk = base + st * C::kStage;
+                        tma_load_4d(sk, &tmk, 0, -bearly, 0, zt, &full[st]);
+                        tma_load_4d(sk + C::kTile, &tmv, 0, -bearly, 0, zt, &full[st]);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+        }
+        return;
+    }
+    // output row (sequence * Hq + query head) of each MMA column, -1 if unused
+    auto row_of = [&](int col) -> int {
+        const int m = col / g;
+        return m < u.count ? u.member[m] * p.num_q_heads + h * g + (col - m * g) : -1;
+    };
+    WarpAttn<D, NT> wa;
+    wa.load_q_rows(static_cast<const __nv_bfloat16 *>(p.q), row_of, lane);
+    wa.reset();
+    const int ncols = min(u.count * g, C::kHeads);
+    grid_consume<C, D, NT, NSTAGE, NCW>(
+        wa, nb,
+        [&](int, int st) {
+            const int2 info = stage_info[st];
+            return info.x < 0 ? make_int3(0, 0, ncols) : make_int3(info.y, info.x * g, info.x * g + g);
+        },
+        p.scale_log2, base, full, empty, ncols, warp, lane, tid, [&](int col, int d, float o, float Mx, float L) {
+            const int r0 = row_of(col);
+            if (r0 < 0) return;
+            const size_t r = (size_t)r0 * p.max_parts + part;
+            p.ws_o[r * D + d] = L > 0.f ? o : 0.f;  // a column this partition never attended leaves an empty state
+            if (d == 0) {
+                p.ws_ml[r * 2 + 0] = Mx;
+                p.ws_ml[r * 2 + 1] = L;
+            }
+        });
+}
+
+// Merges each (sequence, query head) row's partition states (log-sum-exp
+// rule, empty states skipped); a row with none gives zeros. One CTA of D
+// threads per (query head, member slot, group).
+template <int D>
+__global__ void __launch_bounds__(D) cascade_reduce_kernel(const DecodeParams p) {
+    __shared__ float scratch[32];
+    __shared__ UnionUnit u;
+    const int hq = blockIdx.x, m = blockIdx.y, z = blockIdx.z, tid = threadIdx.x;
+    const int s = __ldg(p.group_members + (size_t)z * p.group_size + m);
+    if (s < 0 || s >= p.num_seqs) return;
+    if (tid < 32) union_unit(p, z, u, tid, false);
+    __syncthreads();
+    const int n = (u.total + p.part_blocks - 1) / p.part_blocks;
+    const size_t row = (size_t)s * p.num_q_heads + hq;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) + row * D;
+    const float *ml = p.ws_ml + row * p.max_parts * 2;
+    const float *o = p.ws_o + row * p.max_parts * D;
+    float Mx = -INFINITY;
+    for (int k = tid; k < n; k += D) Mx = fmaxf(Mx, ml[2 * k]);
+    Mx = block_reduce(Mx, true, scratch);
+    if (Mx == -INFINITY) {  // nothing attended: empty context
+        out[tid] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    float W = 0.f, acc = 0.f;
+    for (int k = 0; k < n; ++k) {
+        const float mk = ml[2 * k];
+        if (mk == -INFINITY) continue;
+        const float w = ml[2 * k + 1] * exp2f(mk - Mx);
+        W += w;
+        acc = fmaf(w, o[(size_t)k * D + tid], acc);
+    }
+    out[tid] = __float2bfloat16_rn(acc / W);
+}
+
+// =====================================================================================
 // K1 (fp32): same decomposition on the CUDA cores, for fp32 caches where the
 // result must hold to ~1e-5. One CTA per (partition, kv head, sequence); warp w
 // takes blocks w, w+NCW, ...; lane l owns head-dim elements l, l+32, ...
@@ -900,20 +1183,6 @@ __global__ void __launch_bounds__(NCW * 32) decode_f32_kernel(const DecodeParams
 //   out = sum_p w_p o_p / sum_p w_p.
 // Sequences with a single partition were written by K1 and are skipped.
 // =====================================================================================
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float *scratch) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float w = __shfl_xor_sync(0xffffffffu, v, o);
-        v = is_max ? fmaxf(v, w) : v + w;
-    }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    __syncthreads();
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    v = is_max ? -INFINITY : 0.f;
-    for (int w = 0; w < nw; ++w) v = is_max ? fmaxf(v, scratch[w]) : v + scratch[w];
-    return v;
-}
 
 template <typename OutT, int D, int PG>
 __global__ void __launch_bounds__(D *PG) lse_reduce_kernel(const DecodeParams p) {

@@ -110,6 +110,9 @@ class Layout:
     used_blocks: np.ndarray           # bool [NB]: referenced by some table after the step
     valid_tokens: np.ndarray          # int32 [NB]: tokens a reader may read in each block
     poison_slots: list = field(default_factory=list)   # (block, first_slot) pairs: NaN from slot on
+    # sequences sharing leading blocks (parallel sampling): int32 [groups, members] and [groups]
+    group_members: np.ndarray = field(default_factory=lambda: np.zeros((0, 1), dtype=np.int32))
+    shared_blocks: np.ndarray = field(default_factory=lambda: np.zeros((0,), dtype=np.int32))
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -271,8 +274,10 @@ def _sampling_layout(sp: WorkloadSpec, rng: np.random.Generator) -> Layout:
     poison_block = free[0]
     for s in range(S):
         tables[s, _blocks_for(int(lens[s])):] = poison_block
+    groups = np.arange(S, dtype=np.int32).reshape(P, G)
+    shared = np.full(P, L // BLOCK_SIZE, dtype=np.int32)      # the full prompt blocks every sample shares
     return Layout(sp, lens.astype(np.int32), tables.astype(np.int32), nb, np.array(slots, dtype=np.int64),
-                  np.array(pairs, dtype=np.int64).reshape(-1, 2), used, valid.astype(np.int32), poison)
+                  np.array(pairs, dtype=np.int64).reshape(-1, 2), used, valid.astype(np.int32), poison, groups, shared)
 
 
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
