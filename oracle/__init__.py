@@ -70,6 +70,9 @@ def _load():
             fn.restype = ctypes.c_int
             fn.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_double] + [ctypes.c_int] * 6 + \
                 [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+            pf = lib.oracle_paged_prefill_attention
+            pf.restype = ctypes.c_int
+            pf.argtypes = [ctypes.c_void_p] * 7 + [ctypes.c_double] + [ctypes.c_int] * 8
             _lib = lib
     return _lib
 
@@ -86,8 +89,9 @@ class use_library:
         _load()
         self._saved = _lib
         lib = ctypes.CDLL(self.path)
-        lib.oracle_paged_decode_attention.restype = ctypes.c_int
-        lib.oracle_paged_decode_attention.argtypes = self._saved.oracle_paged_decode_attention.argtypes
+        for name in ("oracle_paged_decode_attention", "oracle_paged_prefill_attention"):
+            getattr(lib, name).restype = ctypes.c_int
+            getattr(lib, name).argtypes = getattr(self._saved, name).argtypes
         _lib = lib
         return lib
 
@@ -153,6 +157,37 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
         int(nthreads or default_threads()))
     if rc != 0:
         raise ValueError(f"oracle_paged_decode_attention failed with code {rc}")
+    return out
+
+
+def paged_prefill_attention(q, k_cache, v_cache, block_tables, context_lens, query_start, scale, num_kv_heads,
+                            nthreads=None) -> np.ndarray:
+    """fp64 causal prefill attention.  q: [total queries, Hq, d] with the
+    queries of sequence s in rows query_start[s] .. query_start[s+1]-1; they
+    are the last n_s tokens of its context_lens[s] cached tokens and query i
+    attends to positions 0 .. context_lens[s] - n_s + i.  Returns float64
+    [total queries, Hq, d]."""
+    q = np.ascontiguousarray(q)
+    k_cache = np.ascontiguousarray(k_cache)
+    v_cache = np.ascontiguousarray(v_cache)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    code = _dtype_code(q)
+    if _dtype_code(k_cache) != code or _dtype_code(v_cache) != code:
+        raise TypeError("q, k_cache and v_cache must share one dtype")
+    TQ, Hq, d = q.shape
+    NB, Hkv, P, d2 = k_cache.shape
+    S = cl.shape[0]
+    if P != BLOCK_SIZE or d2 != d or Hkv != num_kv_heads or qs.shape != (S + 1,) or qs[-1] != TQ or qs[0] != 0:
+        raise ValueError("bad prefill shapes")
+    out = np.zeros((TQ, Hq, d), dtype=np.float64)
+    rc = _load().oracle_paged_prefill_attention(
+        out.ctypes.data, q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data, bt.ctypes.data, cl.ctypes.data,
+        qs.ctypes.data, float(scale), int(num_kv_heads), int(Hq), int(d), int(bt.shape[1]), int(NB), code, int(S),
+        int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_paged_prefill_attention failed with code {rc}")
     return out
 
 

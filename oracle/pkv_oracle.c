@@ -221,3 +221,142 @@ int oracle_paged_decode_attention(double *out, const void *q, const void *k_cach
     free(tid);
     return status;
 }
+
+/*
+ * Causal attention for the prefill of several new tokens per sequence
+ * ("Batching Continuo y PagedAttention" (cruxr.ai), section "Juntándolo todo:
+ * Arquitectura de vLLM": the prefill processes the whole prompt in one
+ * forward pass to fill the KV cache; "Continuous Batching" (ultralytics.com
+ * glossary), section "Cómo funciona la planificación a nivel de iteración":
+ * long prompts are prefilled in chunks).
+ *
+ * Sequence s has context_lens[s] tokens in the cache, the last n_s of which
+ * are its new tokens, n_s = query_start[s+1] - query_start[s]; query row
+ * query_start[s] + i is the token at position context_lens[s] - n_s + i and
+ * attends, causally, to positions 0 .. context_lens[s] - n_s + i. The textbook
+ * definition per query: x_t = scale <q, K_t> over those positions, softmax,
+ * weighted sum of V_t.
+ * q, out: [total queries][num_q_heads][head_dim]; out in double.
+ */
+typedef struct {
+    double *out;
+    const void *q, *k_cache, *v_cache;
+    const int32_t *block_tables, *context_lens, *query_start;
+    double scale;
+    int num_kv_heads, num_q_heads, head_dim, max_blocks_per_seq, num_blocks, dtype, num_seqs;
+    int nthreads, thread_index, status;
+} prefill_job_t;
+
+static void *prefill_worker(void *arg) {
+    prefill_job_t *j = (prefill_job_t *)arg;
+    const int d = j->head_dim, g = j->num_q_heads / j->num_kv_heads;
+    const int maxlen = j->max_blocks_per_seq * PKV_ORACLE_BLOCK;
+    double *K = (double *)malloc((size_t)maxlen * d * sizeof(double));
+    double *V = (double *)malloc((size_t)maxlen * d * sizeof(double));
+    double *x = (double *)malloc((size_t)maxlen * sizeof(double));
+    j->status = ORACLE_OK;
+    if (!K || !V || !x) j->status = ORACLE_ENOMEM;
+    const long units = (long)j->num_seqs * j->num_kv_heads;
+    for (long u = j->thread_index; u < units && j->status == ORACLE_OK; u += j->nthreads) {
+        const int s = (int)(u / j->num_kv_heads), hkv = (int)(u % j->num_kv_heads);
+        const int len = j->context_lens[s];
+        const int q0 = j->query_start[s], n = j->query_start[s + 1] - q0;
+        if (len < 0 || len > maxlen || n < 0 || n > len) {
+            j->status = ORACLE_EINDEX;
+            break;
+        }
+        for (int t = 0; t < len; ++t) {
+            int32_t blk = j->block_tables[(size_t)s * j->max_blocks_per_seq + t / PKV_ORACLE_BLOCK];
+            if (blk < 0 || blk >= j->num_blocks) {
+                j->status = ORACLE_EINDEX;
+                break;
+            }
+            size_t row = (((size_t)blk * j->num_kv_heads + hkv) * PKV_ORACLE_BLOCK + t % PKV_ORACLE_BLOCK) * d;
+            for (int i = 0; i < d; ++i) {
+                K[(size_t)t * d + i] = widen(j->k_cache, row + i, j->dtype);
+                V[(size_t)t * d + i] = widen(j->v_cache, row + i, j->dtype);
+            }
+        }
+        if (j->status != ORACLE_OK) break;
+        for (int qi = 0; qi < n; ++qi) {
+            const int pos = len - n + qi;  /* this query's position: it sees keys 0 .. pos */
+            for (int m = 0; m < g; ++m) {
+                const int hq = hkv * g + m;
+                const size_t qrow = ((size_t)(q0 + qi) * j->num_q_heads + hq) * d;
+                double mx = -INFINITY;
+                for (int t = 0; t <= pos; ++t) {
+                    double dot = 0.0;
+                    for (int i = 0; i < d; ++i) dot += widen(j->q, qrow + i, j->dtype) * K[(size_t)t * d + i];
+                    x[t] = j->scale * dot;
+                    if (x[t] > mx) mx = x[t];
+                }
+                double z = 0.0;
+                for (int t = 0; t <= pos; ++t) {
+                    x[t] = exp(x[t] - mx);
+                    z += x[t];
+                }
+                double *o = j->out + qrow;
+                for (int i = 0; i < d; ++i) o[i] = 0.0;
+                for (int t = 0; t <= pos; ++t) {
+                    const double p = x[t] / z;
+                    for (int i = 0; i < d; ++i) o[i] += p * V[(size_t)t * d + i];
+                }
+            }
+        }
+    }
+    free(K);
+    free(V);
+    free(x);
+    return NULL;
+}
+
+int oracle_paged_prefill_attention(double *out, const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   const int32_t *query_start, double scale, int num_kv_heads, int num_q_heads,
+                                   int head_dim, int max_blocks_per_seq, int num_blocks, int dtype, int num_seqs,
+                                   int nthreads) {
+    if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0) return ORACLE_EARG;
+    if (head_dim <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || num_seqs < 0) return ORACLE_EARG;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return ORACLE_EARG;
+    if (num_seqs == 0) return ORACLE_OK;
+    if (nthreads < 1) nthreads = 1;
+    long units = (long)num_seqs * num_kv_heads;
+    if (nthreads > units) nthreads = (int)units;
+    prefill_job_t *jobs = (prefill_job_t *)calloc((size_t)nthreads, sizeof(prefill_job_t));
+    pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tid) {
+        free(jobs);
+        free(tid);
+        return ORACLE_ENOMEM;
+    }
+    int status = ORACLE_OK, started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        prefill_job_t *j = &jobs[t];
+        j->out = out;
+        j->q = q;
+        j->k_cache = k_cache;
+        j->v_cache = v_cache;
+        j->block_tables = block_tables;
+        j->context_lens = context_lens;
+        j->query_start = query_start;
+        j->scale = scale;
+        j->num_kv_heads = num_kv_heads;
+        j->num_q_heads = num_q_heads;
+        j->head_dim = head_dim;
+        j->max_blocks_per_seq = max_blocks_per_seq;
+        j->num_blocks = num_blocks;
+        j->dtype = dtype;
+        j->num_seqs = num_seqs;
+        j->nthreads = nthreads;
+        j->thread_index = t;
+        if (pthread_create(&tid[t], NULL, prefill_worker, j) != 0) break;
+        ++started;
+    }
+    for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+    if (started < nthreads) status = ORACLE_ENOMEM;
+    for (int t = 0; t < started; ++t)
+        if (jobs[t].status != ORACLE_OK) status = jobs[t].status;
+    free(jobs);
+    free(tid);
+    return status;
+}

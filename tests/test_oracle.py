@@ -341,3 +341,49 @@ def test_copy_blocks_copies_whole_blocks():
     assert np.array_equal(kc, ek) and np.array_equal(vc, ev)
     with pytest.raises(ValueError):
         oracle.copy_blocks(kc, vc, np.array([[0, 5]], np.int64))
+
+
+# --- causal prefill ---------------------------------------------------------------------
+
+def dense_causal_reference(q_rows, K, V, scale, g, n_new):
+    """scipy softmax over each query's visible prefix of dense K/V."""
+    ctx = K.shape[1]
+    out = np.zeros(q_rows.shape, dtype=np.float64)
+    for i in range(n_new):
+        pos = ctx - n_new + i
+        for hq in range(q_rows.shape[1]):
+            Ks = K[hq // g, :pos + 1].astype(np.float64)
+            Vs = V[hq // g, :pos + 1].astype(np.float64)
+            w = scipy.special.softmax(scale * (Ks @ q_rows[i, hq].astype(np.float64)))
+            out[i, hq] = w @ Vs
+    return out
+
+
+@pytest.mark.parametrize("g", [1, 4])
+def test_prefill_matches_dense_causal_bruteforce(g):
+    rng = np.random.default_rng(50 + g)
+    d, Hkv = 64, 2
+    # (context length, new tokens): whole prompts, chunks after earlier context, single tokens
+    shapes = [(1, 1), (17, 17), (40, 9), (33, 1), (64, 64), (100, 37)]
+    K = [rng.standard_normal((Hkv, c, d)).astype(np.float32) for c, _ in shapes]
+    V = [rng.standard_normal((Hkv, c, d)).astype(np.float32) for c, _ in shapes]
+    qs = np.concatenate([[0], np.cumsum([n for _, n in shapes])]).astype(np.int32)
+    q = rng.standard_normal((int(qs[-1]), Hkv * g, d)).astype(np.float32)
+    kc, vc, t, ln = paginate(K, V, 64, rng)
+    got = oracle.paged_prefill_attention(q, kc, vc, t, ln, qs, 0.125, Hkv)
+    for s, (c, n) in enumerate(shapes):
+        ref = dense_causal_reference(q[qs[s]:qs[s + 1]], K[s], V[s], 0.125, g, n)
+        np.testing.assert_allclose(got[qs[s]:qs[s + 1]], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_first_query_sees_only_itself_and_last_query_is_decode():
+    rng = np.random.default_rng(60)
+    d, Hkv, n = 128, 1, 30
+    K = [rng.standard_normal((Hkv, n, d)).astype(np.float32)]
+    V = [rng.standard_normal((Hkv, n, d)).astype(np.float32)]
+    kc, vc, t, ln = paginate(K, V, 8, rng)
+    q = rng.standard_normal((n, 2, d)).astype(np.float32)
+    out = oracle.paged_prefill_attention(q, kc, vc, t, ln, np.array([0, n], np.int32), 0.1, Hkv)
+    assert np.array_equal(out[0, 0], V[0][0, 0].astype(np.float64))      # position 0 attends to itself alone
+    dec = oracle.paged_decode_attention(q[n - 1:n], kc, vc, t, ln, 0.1, Hkv)
+    np.testing.assert_allclose(out[n - 1], dec[0], rtol=0, atol=1e-14)

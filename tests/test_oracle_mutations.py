@@ -22,6 +22,9 @@ MUTATIONS = {
     "strided_gqa": ("const int hq = hkv * g + n;", "const int hq = n * j->num_kv_heads + hkv;"),
     "keys_from_values": ("dot += widen(j->q, qrow + i, j->dtype) * K[(size_t)t * d + i];",
                          "dot += widen(j->q, qrow + i, j->dtype) * V[(size_t)t * d + i];"),
+    "prefill_sees_next_token": ("const int pos = len - n + qi;",
+                                "const int pos = (len - n + qi + 1 < len) ? len - n + qi + 1 : len - 1;"),
+    "prefill_misses_own_token": ("const int pos = len - n + qi;", "const int pos = len - n + qi - 1;"),
     "bf16_low_half": ("uint32_t bits = ((uint32_t)((const uint16_t *)base)[idx]) << 16;",
                       "uint32_t bits = ((uint32_t)((const uint16_t *)base)[idx]) << 15;"),
 }
@@ -35,6 +38,8 @@ PIN_CALLS = [
     lambda: pins.test_matches_dense_bruteforce("f32", 4),
     lambda: pins.test_matches_dense_bruteforce("bf16", 1),
     lambda: pins.test_log_sum_exp_merge_of_partitions_equals_whole(),
+    lambda: pins.test_prefill_matches_dense_causal_bruteforce(1),
+    lambda: pins.test_prefill_first_query_sees_only_itself_and_last_query_is_decode(),
 ]
 
 
