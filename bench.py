@@ -40,6 +40,7 @@ from paged_kv_cache_177_gb300 import workloads as W  # noqa: E402
 METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; µs per decode step"
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -491,7 +492,10 @@ def run_op(args, rank, world, local, dist):
     --op append_layers: kv_append of one token per sequence into every layer's
       caches (40 layers) in one launch, against one launch per layer.
     --op shared_prefix: shared-prefix decode on a workload with shared
-      prompts, against plain decode of the same batch."""
+      prompts, against plain decode of the same batch.
+    --op prefill: a prefill step (multi-token kv_append of every new token,
+      then causal prefill attention) on --prefill-workload; TFLOP/s of the
+      attention against the measured bf16 tensor peak."""
     from paged_kv_cache_177_gb300 import build
     build.build_library()
     from paged_kv_cache_177_gb300 import binding as B
@@ -500,6 +504,8 @@ def run_op(args, rank, world, local, dist):
         return
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.op == "prefill":
+        return run_prefill(args, dev, B)
     sp = W.spec(args.workload)
     w = W.make_workload(sp, device=dev)
     lay = w.layout
@@ -610,6 +616,75 @@ def run_op(args, rank, world, local, dist):
     print(json.dumps(line), flush=True)
 
 
+def graph_time(fn, n, dev, evict):
+    """Median device time of fn, captured once as a CUDA graph and replayed
+    after an L2 eviction each time."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        fn()                                   # warm-up outside the capture
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        fn()
+    stream = torch.cuda.current_stream(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        evict.sum()
+        evs[i][0].record(stream)
+        g.replay()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    t = sorted(a.elapsed_time(b) for a, b in evs)
+    return t[len(t) // 2] / 1e3
+
+
+def tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def run_prefill(args, dev, B):
+    w = W.make_prefill(args.prefill_workload, device=dev)
+    sp = w.spec
+    evict = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev).fill_(1.0)
+    out = torch.empty_like(w.q)
+    mq, mc = w.max_query_len, w.max_context_len
+
+    def attention():
+        B.paged_prefill_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.query_start,
+                                  w.scale, max_query_len=mq, max_context_len=mc)
+
+    def step():
+        B.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
+        attention()
+
+    n = args.steps or 30
+    t_step = graph_time(step, n, dev, evict)
+    t_attn = graph_time(attention, n, dev, evict)
+    T = int(w.q.shape[0])
+    flops = w.flops()
+    peak, kind = tensor_peak()
+    tflops = flops / t_attn / 1e12
+    line = {"metric": "prefill attention TFLOP/s (causal, algorithmic FLOPs)", "unit": "TFLOP/s",
+            "value": round(tflops, 2), "tokens_per_s": round(T / t_step, 1),
+            "attention": {"us": round(t_attn * 1e6, 2), "TFLOP/s": round(tflops, 2),
+                          "frac_of_peak": round(tflops / peak, 4)},
+            "step": {"us": round(t_step * 1e6, 2), "what": "kv_append of every new token + prefill attention"},
+            "flops": int(flops), "new_tokens": T, "peak": peak, "peak_kind": kind, "bound": "tensor",
+            "higher_is_better": True,
+            "timing": "each variant captured once as a CUDA graph, median of replays after an L2 eviction",
+            "config": {"workload": f"{sp.name}: {sp.num_seqs} seqs, {sp.num_q_heads} q / {sp.num_kv_heads} kv "
+                                   f"heads, head_dim {sp.head_dim}, bf16, block 16, new tokens {sp.new_lengths} "
+                                   f"[{sp.new_lo}, {sp.new_hi}], prior context [{sp.prior_lo}, {sp.prior_hi}]"},
+            "op": "prefill", "n_gpus": 1, "dtype": "bf16", "data": "synthetic"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -622,7 +697,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", choices=["step", "swap", "append_layers", "shared_prefix"], default="step",
+    ap.add_argument("--prefill-workload", default="prefill13b", choices=list(W.PREFILL_SPECS))
+    ap.add_argument("--op", choices=["step", "swap", "append_layers", "shared_prefix", "prefill"], default="step",
                     help="step: the decode step (the benchmark line); swap / append_layers: secondary measurements")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -48,6 +48,8 @@ _decode = _decl("paged_decode_attention", _i, _vp, _vp, _vp, _vp, _vp, _vp, _f, 
                 _vp, _sz, _vp)
 _shared = _decl("paged_decode_attention_shared_prefix", _i, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i,
                 _i, _i, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp)
+_prefill = _decl("paged_prefill_attention", _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i,
+                 _i, _i, _vp)
 _shared_ws = _decl("pkv_shared_prefix_workspace_bytes", _sz, _i, _i, _i, _i, _i, _i)
 _append = _decl("kv_append", _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
 _copy = _decl("copy_blocks", _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
@@ -241,6 +243,45 @@ def paged_decode_attention_shared_prefix(out: torch.Tensor, q: torch.Tensor, k_c
                    Hq, D, block_tables.shape[1], NB, int(max_context_len), _p(group_members) if G else None,
                    _p(shared_blocks) if G else None, G, max(M, 1), PKV_BF16, int(partition_tokens), _p(workspace),
                    ws_bytes, _stream_ptr(dev, stream)), "paged_decode_attention_shared_prefix")
+    return out
+
+
+def paged_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor, query_start: torch.Tensor,
+                            scale: float, *, max_query_len: Optional[int] = None,
+                            max_context_len: Optional[int] = None,
+                            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Causal attention of each sequence's last n_s context tokens (a prompt
+    or a chunk of one, already appended to the cache); see include/pagedkv.h.
+
+    q, out: bf16 [T, Hq, D], sequence s owning rows query_start[s] ..
+    query_start[s+1]-1; query_start int32 [S + 1]; caches, tables and lengths
+    as for ``paged_decode_attention``.  ``max_query_len`` and
+    ``max_context_len`` default to the maxima of the device arrays (a sync).
+    """
+    dev = _dev(out, q, k_cache, v_cache, block_tables, context_lens, query_start)
+    if q.dtype != torch.bfloat16 or not (out.dtype == k_cache.dtype == v_cache.dtype == q.dtype):
+        raise TypeError("prefill attention is bf16")
+    if query_start.dtype != torch.int32 or context_lens.dtype != torch.int32 or block_tables.dtype != torch.int32:
+        raise TypeError("query_start, context_lens and block_tables are int32")
+    if q.dim() != 3 or out.shape != q.shape or not (q.is_contiguous() and out.is_contiguous()):
+        raise ValueError("q and out must be contiguous [T, Hq, D]")
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous() and block_tables.is_contiguous()):
+        raise ValueError("caches and block tables must be contiguous")
+    S = context_lens.shape[0]
+    if query_start.shape != (S + 1,):
+        raise ValueError("query_start must be [S + 1]")
+    _, Hq, D = q.shape
+    NB, Hkv, P, _ = k_cache.shape
+    if P != BLOCK_SIZE or k_cache.shape[3] != D or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must be [NB, Hkv, 16, D] with q's head_dim")
+    if max_query_len is None:
+        max_query_len = int((query_start[1:] - query_start[:-1]).max().item()) if S else 0
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    _check(_prefill(_p(out), _p(q), _p(k_cache), _p(v_cache), _p(block_tables), _p(context_lens), _p(query_start),
+                    float(scale), Hkv, S, Hq, D, block_tables.shape[1] if S else 1, NB, int(max_query_len),
+                    int(max_context_len), PKV_BF16, _stream_ptr(dev, stream)), "paged_prefill_attention")
     return out
 
 

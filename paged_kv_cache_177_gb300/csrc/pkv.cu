@@ -36,7 +36,11 @@ constexpr int kMaxParts = 8192;        // partitions per sequence the reduce ker
 #ifndef PKV_PERSIST_STAGES_D64
 #define PKV_PERSIST_STAGES_D64 2
 #endif
+#ifndef PKV_PREFILL_STAGES
+#define PKV_PREFILL_STAGES 4
+#endif
 constexpr int kNstage = PKV_GRID_STAGES;
+constexpr int kPrefillStages = PKV_PREFILL_STAGES;
 constexpr int kNcw = PKV_GRID_CONSUMERS;
 // persistent bf16 kernel: one CTA of kPersistWarps warps per SM
 constexpr int kPersistWarps = PKV_PERSIST_WARPS;
@@ -154,6 +158,23 @@ int launch_reduce(const pkv::DecodeParams &p, pkv_dtype dt, cudaStream_t st) {
     return check_launch();
 }
 
+
+template <int D>
+int launch_prefill(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::PrefillParams &pp, dim3 grid,
+                   cudaStream_t st) {
+    using C = pkv::PrefillCfg<D, kPrefillStages>;
+    auto kern = pkv::prefill_bf16_kernel<D, kPrefillStages>;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (configured_device != dev) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured_device = dev;
+    }
+    kern<<<grid, C::kThreads, C::kSmem, st>>>(tmk, tmv, pp);
+    return check_launch();
+}
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -477,6 +498,57 @@ int paged_decode_attention_shared_prefix(void *out, const void *q, const void *k
     if (head_dim == 128)
         return wide ? launch_cascade<128, 2>(tmk, tmv, p, grid, st) : launch_cascade<128, 1>(tmk, tmv, p, grid, st);
     return wide ? launch_cascade<64, 2>(tmk, tmv, p, grid, st) : launch_cascade<64, 1>(tmk, tmv, p, grid, st);
+}
+
+int paged_prefill_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *context_lens, const int32_t *query_start,
+                            float scale, int num_kv_heads, int num_seqs, int num_q_heads, int head_dim,
+                            int max_blocks_per_seq, int num_blocks, int max_query_len, int max_context_len,
+                            pkv_dtype dtype, void *stream) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+        max_context_len < 0 || max_query_len < 0)
+        return PKV_ERR_ARG;
+    if (dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0) return PKV_ERR_ARG;
+    const int g = num_q_heads / num_kv_heads;
+    if (g > 64) return PKV_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return PKV_ERR_ARG;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)num_blocks * num_kv_heads * 16 >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+    const int tile_tokens = 64 / g;
+    const int tiles = (max_query_len + tile_tokens - 1) / tile_tokens;
+    if (tiles > (1 << 30)) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || max_query_len == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start) return PKV_ERR_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+
+    pkv::PrefillParams pp{};
+    pkv::DecodeParams &p = pp.d;
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = g;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.max_context_len = max_context_len;
+    pp.query_start = query_start;
+    pp.tile_tokens = tile_tokens;
+    pp.max_query_len = max_query_len;
+    alignas(64) CUtensorMap tmk, tmv;
+    int rc;
+    if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
+    if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
+    const dim3 grid(tiles, num_kv_heads, num_seqs);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return head_dim == 128 ? launch_prefill<128>(tmk, tmv, pp, grid, st) : launch_prefill<64>(tmk, tmv, pp, grid, st);
 }
 
 int pkv_check_copy_pairs(const int64_t *host_pairs, int num_pairs, int num_blocks) {

@@ -371,3 +371,169 @@ def from_numpy_bits(a: np.ndarray, device="cpu") -> torch.Tensor:
     if a.dtype == np.uint16:
         return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(device)
     return torch.from_numpy(a.copy()).to(device)
+
+
+# ---- prefill steps ------------------------------------------------------------------------
+#
+# A prefill step writes n_s new tokens per sequence into the cache (a whole
+# prompt, or a chunk of one after `prior` tokens already cached) and attends
+# each new token causally over the sequence's tokens up to itself.
+#
+# =============  =====  =========  ====  =====================================  ==================
+# name           seqs   Hq / Hkv   d     new tokens n_s                         prior context
+# =============  =====  =========  ====  =====================================  ==================
+# prefill13b     32     40 / 40    128   lognormal(ln 500, 0.8) in [16, 2048]   0 (whole prompts)
+# chunked_gqa    16     32 / 8     128   uniform int [1, 512]                   uniform [0, 2048]
+# =============  =====  =========  ====  =====================================  ==================
+
+@dataclass(frozen=True)
+class PrefillSpec:
+    name: str
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    new_lengths: str                # "lognormal", "uniform" or "explicit"
+    new_lo: int
+    new_hi: int
+    new_median: float = 0.0
+    new_sigma: float = 0.0
+    prior_lo: int = 0
+    prior_hi: int = 0
+    pool_factor: float = 1.1
+    seed: int = 0
+    new_list: tuple = ()            # explicit n_s
+    prior_list: tuple = ()          # explicit prior context (with new_list)
+
+
+PREFILL_SPECS = {
+    "prefill13b": PrefillSpec("prefill13b", 32, 40, 40, 128, "lognormal", 16, 2048, 500.0, 0.8, seed=2001),
+    "chunked_gqa": PrefillSpec("chunked_gqa", 16, 32, 8, 128, "uniform", 1, 512, prior_lo=0, prior_hi=2048,
+                               seed=2002),
+}
+
+
+@dataclass
+class PrefillWorkload:
+    """One prefill step, on ``device``: kv_append of ``k_new``/``v_new`` at
+    ``slot_mapping`` (every new token of every sequence, in query order), then
+    causal attention of ``q`` over the cache."""
+    spec: PrefillSpec
+    q: torch.Tensor               # bf16 [T, Hq, d]
+    k_cache: torch.Tensor         # bf16 [NB, Hkv, 16, d]; new-token slots NaN before the append
+    v_cache: torch.Tensor
+    k_new: torch.Tensor           # bf16 [T, Hkv, d]
+    v_new: torch.Tensor
+    slot_mapping: torch.Tensor    # int64 [T]
+    block_tables: torch.Tensor    # int32 [S, maxB]
+    context_lens: torch.Tensor    # int32 [S] = prior + n_s
+    query_start: torch.Tensor     # int32 [S + 1]
+    scale: float
+    host: dict                    # numpy copies of the index arrays
+
+    @property
+    def max_query_len(self) -> int:
+        n = np.diff(self.host["query_start"])
+        return int(n.max()) if n.size else 0
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.host["context_lens"].max()) if self.host["context_lens"].size else 0
+
+    def pairs(self) -> int:
+        """(query, key) pairs the causal attention scores, per query head."""
+        n = np.diff(self.host["query_start"]).astype(np.int64)
+        prior = self.host["context_lens"].astype(np.int64) - n
+        return int(np.sum(n * prior + n * (n + 1) // 2))
+
+    def flops(self) -> int:
+        """Algorithmic FLOPs: 2 d for q.k and 2 d for p v per scored pair and query head."""
+        return 4 * self.spec.head_dim * self.spec.num_q_heads * self.pairs()
+
+    def to(self, device) -> "PrefillWorkload":
+        f = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in self.__dict__.items()}
+        return PrefillWorkload(**f)
+
+
+def prefill_spec(name: str, **overrides) -> PrefillSpec:
+    s = PREFILL_SPECS[name]
+    if "new_list" in overrides:
+        overrides.setdefault("new_lengths", "explicit")
+        overrides.setdefault("num_seqs", len(overrides["new_list"]))
+    return dataclasses.replace(s, **overrides) if overrides else s
+
+
+def make_prefill(name_or_spec, device="cpu", **overrides) -> PrefillWorkload:
+    sp = prefill_spec(name_or_spec, **overrides) if isinstance(name_or_spec, str) else name_or_spec
+    rng = np.random.default_rng(sp.seed)
+    S = sp.num_seqs
+    if sp.new_lengths == "explicit":
+        new = np.array(sp.new_list, dtype=np.int64)
+        prior = np.array(sp.prior_list or (0,) * S, dtype=np.int64)
+        if len(new) != S or len(prior) != S:
+            raise ValueError("new_list and prior_list need one entry per sequence")
+    else:
+        if sp.new_lengths == "lognormal":
+            raw = rng.lognormal(mean=math.log(sp.new_median), sigma=sp.new_sigma, size=S)
+            new = np.clip(np.rint(raw), sp.new_lo, sp.new_hi).astype(np.int64)
+        elif sp.new_lengths == "uniform":
+            new = rng.integers(sp.new_lo, sp.new_hi + 1, size=S).astype(np.int64)
+        else:
+            raise ValueError(sp.new_lengths)
+        prior = rng.integers(sp.prior_lo, sp.prior_hi + 1, size=S).astype(np.int64)
+    lens = prior + new
+    need = np.array([_blocks_for(int(n)) for n in lens], dtype=np.int64)
+    total = int(need.sum())
+    nb = max(int(math.ceil(sp.pool_factor * total)), total + 1)
+    perm = rng.permutation(nb)
+    max_b = max(int(need.max()) if S else 1, 1)
+    tables = np.empty((S, max_b), dtype=np.int64)
+    used = np.zeros(nb, dtype=bool)
+    pos = 0
+    for s in range(S):
+        tables[s, :need[s]] = perm[pos:pos + need[s]]
+        used[perm[pos:pos + need[s]]] = True
+        pos += need[s]
+    poison_block = int(perm[pos])
+    for s in range(S):
+        tables[s, need[s]:] = poison_block
+    slots = []
+    for s in range(S):
+        for t in range(int(prior[s]), int(lens[s])):
+            slots.append(int(tables[s, t // BLOCK_SIZE]) * BLOCK_SIZE + t % BLOCK_SIZE)
+    slots = np.array(slots, dtype=np.int64)
+    qs = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    T = int(qs[-1])
+    gen = torch.Generator(device=device)
+    gen.manual_seed(sp.seed)
+    Hq, Hkv, d = sp.num_q_heads, sp.num_kv_heads, sp.head_dim
+    dt = torch.bfloat16
+    q = _randn((T, Hq, d), dt, gen, device)
+    k_cache = _randn((nb, Hkv, BLOCK_SIZE, d), dt, gen, device)
+    v_cache = _randn((nb, Hkv, BLOCK_SIZE, d), dt, gen, device)
+    k_new = _randn((T, Hkv, d), dt, gen, device)
+    v_new = _randn((T, Hkv, d), dt, gen, device)
+    # poison: unreferenced blocks, slots past each sequence's end, the new tokens' slots
+    unused = torch.from_numpy(np.nonzero(~used)[0]).to(device)
+    for c in (k_cache, v_cache):
+        if unused.numel():
+            sub = c.index_select(0, unused)
+            _nan_fill(sub, "bf16")
+            c.index_copy_(0, unused, sub)
+        for s in range(S):
+            if lens[s] % BLOCK_SIZE:
+                _nan_fill(c[int(tables[s, need[s] - 1]), :, int(lens[s] % BLOCK_SIZE):, :], "bf16")
+        if slots.size:
+            flat = c.view(nb * 1, Hkv, BLOCK_SIZE, d)
+            idx = torch.from_numpy(slots).to(device)
+            blk, off = idx // BLOCK_SIZE, idx % BLOCK_SIZE
+            flat[blk, :, off, :] = float("nan")
+    host = {"block_tables": tables.astype(np.int32), "context_lens": lens.astype(np.int32), "query_start": qs,
+            "slot_mapping": slots, "num_blocks": nb}
+    return PrefillWorkload(
+        spec=sp, q=q, k_cache=k_cache, v_cache=v_cache, k_new=k_new, v_new=v_new,
+        slot_mapping=torch.from_numpy(slots.copy()).to(device),
+        block_tables=torch.from_numpy(host["block_tables"].copy()).to(device),
+        context_lens=torch.from_numpy(host["context_lens"].copy()).to(device),
+        query_start=torch.from_numpy(qs.copy()).to(device),
+        scale=1.0 / math.sqrt(d), host=host)
