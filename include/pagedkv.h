@@ -196,22 +196,23 @@ size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int head
  * sequence's tokens at positions 0 .. pos:
  *   out[r][hq][:] = sum_{t<=pos} softmax_t(scale * q[r][hq] . K_t[hkv]) V_t[hkv],
  *   hkv = hq / (num_q_heads / num_kv_heads).
- * q, out: bf16 [total_queries][num_q_heads][head_dim], total_queries =
- *   query_start[num_seqs]; caches, block_tables, context_lens as for
- *   paged_decode_attention. query_start: int32 [num_seqs + 1], device,
- *   non-decreasing from 0.
+ * q, out: bf16 [num_queries][num_q_heads][head_dim]; caches, block_tables,
+ *   context_lens as for paged_decode_attention. query_start: int32
+ *   [num_seqs + 1], device, non-decreasing from 0, query_start[num_seqs] <=
+ *   num_queries.
  * max_query_len: host-side upper bound on every n_s (sizes the launch);
  *   max_context_len as for paged_decode_attention.
- * n_s < 0, n_s > context_lens[s] or n_s > max_query_len: the sequence's rows
- *   are left unwritten and PKV_DEVERR_LENGTH is raised.
+ * n_s < 0, n_s > context_lens[s], n_s > max_query_len or rows past
+ *   num_queries: the sequence's rows are left unwritten and PKV_DEVERR_LENGTH
+ *   is raised.
  * bf16 only; head_dim 64 or 128; num_q_heads / num_kv_heads at most 64.
  * No workspace; one launch.
  */
 int paged_prefill_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *block_tables, const int32_t *context_lens, const int32_t *query_start,
                             float scale, int num_kv_heads, int num_seqs, int num_q_heads, int head_dim,
-                            int max_blocks_per_seq, int num_blocks, int max_query_len, int max_context_len,
-                            pkv_dtype dtype, void *stream);
+                            int max_blocks_per_seq, int num_blocks, int num_queries, int max_query_len,
+                            int max_context_len, pkv_dtype dtype, void *stream);
 
 /*
  * KV append: for each token t with slot = slot_mapping[t] >= 0,

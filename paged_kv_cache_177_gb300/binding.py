@@ -49,7 +49,7 @@ _decode = _decl("paged_decode_attention", _i, _vp, _vp, _vp, _vp, _vp, _vp, _f, 
 _shared = _decl("paged_decode_attention_shared_prefix", _i, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i,
                 _i, _i, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp)
 _prefill = _decl("paged_prefill_attention", _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i,
-                 _i, _i, _vp)
+                 _i, _i, _i, _vp)
 _shared_ws = _decl("pkv_shared_prefix_workspace_bytes", _sz, _i, _i, _i, _i, _i, _i)
 _append = _decl("kv_append", _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
 _copy = _decl("copy_blocks", _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
@@ -280,8 +280,9 @@ def paged_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.T
     if max_context_len is None:
         max_context_len = int(context_lens.max().item()) if S else 0
     _check(_prefill(_p(out), _p(q), _p(k_cache), _p(v_cache), _p(block_tables), _p(context_lens), _p(query_start),
-                    float(scale), Hkv, S, Hq, D, block_tables.shape[1] if S else 1, NB, int(max_query_len),
-                    int(max_context_len), PKV_BF16, _stream_ptr(dev, stream)), "paged_prefill_attention")
+                    float(scale), Hkv, S, Hq, D, block_tables.shape[1] if S else 1, NB, q.shape[0],
+                    int(max_query_len), int(max_context_len), PKV_BF16, _stream_ptr(dev, stream)),
+           "paged_prefill_attention")
     return out
 
 

@@ -14,6 +14,7 @@
 
 #include "pagedkv.h"
 #include "pkv_kernels.cuh"
+#include "pkv_prefill_tc.cuh"
 
 namespace {
 
@@ -36,11 +37,8 @@ constexpr int kMaxParts = 8192;        // partitions per sequence the reduce ker
 #ifndef PKV_PERSIST_STAGES_D64
 #define PKV_PERSIST_STAGES_D64 2
 #endif
-#ifndef PKV_PREFILL_STAGES
-#define PKV_PREFILL_STAGES 4
-#endif
 constexpr int kNstage = PKV_GRID_STAGES;
-constexpr int kPrefillStages = PKV_PREFILL_STAGES;
+
 constexpr int kNcw = PKV_GRID_CONSUMERS;
 // persistent bf16 kernel: one CTA of kPersistWarps warps per SM
 constexpr int kPersistWarps = PKV_PERSIST_WARPS;
@@ -85,14 +83,36 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // the 128-byte swizzle on each 128-byte row. Loading from y = valid - 16
 // makes TMA zero-fill the rows before the tile start: that is how the last
 // block of a sequence arrives with its slots past the end already zero.
-int encode_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int num_kv_heads, int head_dim) {
+int encode_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int num_kv_heads, int head_dim,
+                     bool one_half = false) {
     auto fn = encode_fn();
     if (!fn) return PKV_ERR_CUDA;
     cuuint64_t dims[4] = {64, 16, (cuuint64_t)head_dim / 64, (cuuint64_t)num_blocks * num_kv_heads};
     cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, 128, (cuuint64_t)head_dim * 2 * 16};
-    cuuint32_t box[4] = {64, 16, (cuuint32_t)head_dim / 64, 1};
+    cuuint32_t box[4] = {64, 16, one_half ? 1u : (cuuint32_t)head_dim / 64, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// (one_half: a box of one 64-element half of the 16 slots' rows, 2 KiB, so a
+// caller can place the halves of consecutive blocks apart.)
+
+// 4-D view of q [T][Hq][D] for the tensor-core prefill: x = element within a
+// 64-element half row, y = half, z = query head, w = query row (token). The
+// box {64, 1, g, tokens} lands one half of a (token, head) tile as rows
+// token * g + head of 128 bytes, with the 128-byte swizzle.
+int encode_q_map(CUtensorMap *map, const void *q, int num_queries, int num_q_heads, int head_dim, int g,
+                 int tokens) {
+    auto fn = encode_fn();
+    if (!fn) return PKV_ERR_CUDA;
+    cuuint64_t dims[4] = {64, (cuuint64_t)head_dim / 64, (cuuint64_t)num_q_heads, (cuuint64_t)num_queries};
+    cuuint64_t strides[3] = {128, (cuuint64_t)head_dim * 2, (cuuint64_t)num_q_heads * head_dim * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)g, (cuuint32_t)tokens};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
@@ -160,10 +180,11 @@ int launch_reduce(const pkv::DecodeParams &p, pkv_dtype dt, cudaStream_t st) {
 
 
 template <int D>
-int launch_prefill(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::PrefillParams &pp, dim3 grid,
-                   cudaStream_t st) {
-    using C = pkv::PrefillCfg<D, kPrefillStages>;
-    auto kern = pkv::prefill_bf16_kernel<D, kPrefillStages>;
+int launch_prefill_tc(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                      const pkv::PrefillParams &pp, dim3 grid, cudaStream_t st) {
+    using C = pkv::TcCfg<D>;
+    static_assert(C::kSmem <= (int)kSmemLimit, "shared memory");
+    auto kern = pkv::prefill_tc_kernel<D>;
     static thread_local int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -172,9 +193,10 @@ int launch_prefill(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::Pr
             return PKV_ERR_CUDA;
         configured_device = dev;
     }
-    kern<<<grid, C::kThreads, C::kSmem, st>>>(tmk, tmv, pp);
+    kern<<<grid, C::kThreads, C::kSmem, st>>>(tmq, tmk, tmv, pp);
     return check_launch();
 }
+
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -503,10 +525,10 @@ int paged_decode_attention_shared_prefix(void *out, const void *q, const void *k
 int paged_prefill_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *block_tables, const int32_t *context_lens, const int32_t *query_start,
                             float scale, int num_kv_heads, int num_seqs, int num_q_heads, int head_dim,
-                            int max_blocks_per_seq, int num_blocks, int max_query_len, int max_context_len,
-                            pkv_dtype dtype, void *stream) {
+                            int max_blocks_per_seq, int num_blocks, int num_queries, int max_query_len,
+                            int max_context_len, pkv_dtype dtype, void *stream) {
     if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
-        max_context_len < 0 || max_query_len < 0)
+        max_context_len < 0 || max_query_len < 0 || num_queries < 0)
         return PKV_ERR_ARG;
     if (dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
@@ -516,10 +538,10 @@ int paged_prefill_attention(void *out, const void *q, const void *k_cache, const
     if (!std::isfinite(scale)) return PKV_ERR_ARG;
     if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
     if ((int64_t)num_blocks * num_kv_heads * 16 >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
-    const int tile_tokens = 64 / g;
+    const int tile_tokens = 128 / g;  // 128 query rows per tile, two tiles per CTA
     const int tiles = (max_query_len + tile_tokens - 1) / tile_tokens;
-    if (tiles > (1 << 30)) return PKV_ERR_UNSUPPORTED;
-    if (num_seqs == 0 || max_query_len == 0) return PKV_OK;
+    const int pairs = (tiles + 1) / 2;
+    if (num_seqs == 0 || max_query_len == 0 || num_queries == 0) return PKV_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start) return PKV_ERR_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
 
@@ -542,13 +564,17 @@ int paged_prefill_attention(void *out, const void *q, const void *k_cache, const
     pp.query_start = query_start;
     pp.tile_tokens = tile_tokens;
     pp.max_query_len = max_query_len;
+    pp.num_queries = num_queries;
     alignas(64) CUtensorMap tmk, tmv;
     int rc;
-    if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
-    if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
-    const dim3 grid(tiles, num_kv_heads, num_seqs);
+    const dim3 grid(pairs, num_kv_heads, num_seqs);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return head_dim == 128 ? launch_prefill<128>(tmk, tmv, pp, grid, st) : launch_prefill<64>(tmk, tmv, pp, grid, st);
+    alignas(64) CUtensorMap tmq;
+    if ((rc = encode_q_map(&tmq, q, num_queries, num_q_heads, head_dim, g, tile_tokens)) != PKV_OK) return rc;
+    if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim, true)) != PKV_OK) return rc;
+    if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim, true)) != PKV_OK) return rc;
+    return head_dim == 128 ? launch_prefill_tc<128>(tmq, tmk, tmv, pp, grid, st)
+                           : launch_prefill_tc<64>(tmq, tmk, tmv, pp, grid, st);
 }
 
 int pkv_check_copy_pairs(const int64_t *host_pairs, int num_pairs, int num_blocks) {

@@ -1105,244 +1105,15 @@ __global__ void __launch_bounds__(D) cascade_reduce_kernel(const DecodeParams p)
     out[tid] = __float2bfloat16_rn(acc / W);
 }
 
-// =====================================================================================
-// Prefill (bf16): causal attention for several new tokens per sequence, the
-// prefill of a prompt or of a chunk of it ("Batching Continuo y
-// PagedAttention", cruxr.ai, section "Juntándolo todo: Arquitectura de vLLM";
-// "Continuous Batching", ultralytics.com glossary, chunked prefill). Sequence
-// s's new tokens are the last n_s of its context_lens[s] cached tokens; query
-// i attends to positions 0 .. context_lens[s] - n_s + i.
-//
-// One CTA per (query tile, kv head, sequence): 64 query rows -- the g query
-// heads of the kv head for 64/g consecutive new tokens -- 16 per consumer
-// warp. The producer warp stages every K/V tile the tile's last query can see
-// (TMA, as in decode) and all four consumer warps read it: per tile and warp
-// S = Q K^T (16 rows x 16 keys, mma m16n8k16 with Q in registers), an online
-// softmax per row with the causal and end-of-context masks, and O += P V with
-// P kept in registers as the A operand. A warp skips the compute of tiles
-// past its own last query.
-// =====================================================================================
-template <int D, int NSTAGE>
-struct PrefillCfg {
-    static constexpr int kNcw = 4;
-    static constexpr int kRows = 16 * kNcw;
-    static constexpr int kSubBytes = kBlock * 128;
-    static constexpr int kTile = kBlock * D * 2;
-    static constexpr int kStage = 2 * kTile;
-    static constexpr int kSteps = D / 16;
-    static constexpr int kThreads = (kNcw + 1) * 32;
-    static constexpr int kBarOffset = NSTAGE * kStage;
-    static constexpr int kSmem = kBarOffset + 2 * NSTAGE * 8 + 1024;
-};
-
+// Prefill (bf16) parameters: causal attention for several new tokens per
+// sequence (the kernel is in pkv_prefill_tc.cuh).
 struct PrefillParams {
     DecodeParams d;
     const int32_t *query_start;  // [S + 1]
-    int tile_tokens;             // query tokens per CTA (64 / g)
+    int tile_tokens;             // query tokens per CTA (16 x consumer warps / g)
     int max_query_len;           // the grid covers this many new tokens per sequence
+    int num_queries;             // rows of q and out
 };
-
-template <int D, int NSTAGE>
-__global__ void __launch_bounds__(PrefillCfg<D, NSTAGE>::kThreads)
-    prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                        const PrefillParams pp) {
-    using C = PrefillCfg<D, NSTAGE>;
-    const DecodeParams &p = pp.d;
-    extern __shared__ uint8_t smem_raw[];
-    const int h = blockIdx.y, s = blockIdx.z;
-    const int tile = gridDim.x - 1 - blockIdx.x;  // the longest (last) tiles start first
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = p.group;
-    const int q0 = __ldg(pp.query_start + s), n = __ldg(pp.query_start + s + 1) - q0;
-    const int len = seq_len(p, s, tid == 0 && blockIdx.x == 0 && h == 0);
-    const int t0 = tile * pp.tile_tokens;
-    if (n < 0 || n > len || n > pp.max_query_len) {  // more new tokens than the context or the grid holds
-        if (tid == 0 && blockIdx.x == 0 && h == 0) raise_error(PKV_DEVERR_LENGTH);
-        return;
-    }
-    if (t0 >= n) return;
-    const int t_end = min(n, t0 + pp.tile_tokens);  // tokens t0 .. t_end - 1
-    const int first_pos = len - n;                  // position of new token 0
-    const int nb = (first_pos + t_end - 1) / kBlock + 1;  // tiles the last query can see
-    const int nblk = (len + kBlock - 1) / kBlock;
-    const int last_valid = len - (nblk - 1) * kBlock;
-
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(base + C::kBarOffset);
-    uint64_t *empty = full + NSTAGE;
-    if (tid == 0) {
-        prefetch_tensormap(&tmk);
-        prefetch_tensormap(&tmv);
-        for (int i = 0; i < NSTAGE; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], C::kNcw);  // every consumer warp reads every tile
-        }
-        mbar_fence_init();
-    }
-    __syncthreads();
-    if (warp == C::kNcw) {
-        grid_produce<C, NSTAGE>(tmk, tmv, p.block_tables + (size_t)s * p.max_blocks_per_seq, 0, nb, nblk - 1,
-                                last_valid, p.num_blocks, p.num_kv_heads, h, base, full, empty, lane);
-        return;
-    }
-
-    // ---- this warp's 16 query rows: row r -> token t0 + r / g, head r % g ----
-    const int gq = lane >> 2, t4 = lane & 3;
-    const int r_lo = warp * 16;
-    auto row_pos = [&](int r) -> int {  // query position of tile row r, or -1 when the row is unused
-        const int t = t0 + r / g;
-        return (r < pp.tile_tokens * g && t < t_end) ? first_pos + t : -1;
-    };
-    const int pos_a = row_pos(r_lo + gq), pos_b = row_pos(r_lo + gq + 8);
-    int warp_last = -1;  // the warp's last query position
-    for (int r = r_lo; r < r_lo + 16; ++r) warp_last = max(warp_last, row_pos(r));
-
-    uint32_t qa[C::kSteps][4];
-    {
-        const __nv_bfloat16 *qb = static_cast<const __nv_bfloat16 *>(p.q);
-        auto qrow = [&](int r) -> const uint32_t * {
-            const int t = t0 + r / g;
-            return reinterpret_cast<const uint32_t *>(qb + ((size_t)(q0 + t) * p.num_q_heads + h * g + r % g) * D);
-        };
-        const uint32_t *ra = pos_a >= 0 ? qrow(r_lo + gq) : nullptr;
-        const uint32_t *rb = pos_b >= 0 ? qrow(r_lo + gq + 8) : nullptr;
-#pragma unroll
-        for (int kk = 0; kk < C::kSteps; ++kk) {
-            const int c = (16 * kk + 2 * t4) / 2;
-            qa[kk][0] = ra ? __ldg(ra + c) : 0u;
-            qa[kk][1] = rb ? __ldg(rb + c) : 0u;
-            qa[kk][2] = ra ? __ldg(ra + c + 4) : 0u;
-            qa[kk][3] = rb ? __ldg(rb + c + 4) : 0u;
-        }
-    }
-    float o[D / 8][4];
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-    const int mi = lane >> 3, r8 = lane & 7;
-
-    for (int j = 0; j < nb; ++j) {
-        const int st = j % NSTAGE;
-        if (!mbar_wait(&full[st], (j / NSTAGE) & 1)) {
-            raise_error(PKV_DEVERR_TIMEOUT);
-            break;
-        }
-        const int lo = (j == nblk - 1) ? kBlock - last_valid : 0;  // rows loaded early (zero-filled)
-        if (j * kBlock > warp_last) {  // every key of this tile is in this warp's future
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
-            continue;
-        }
-        const uint32_t sk = smem_u32(base + st * C::kStage), sv = sk + C::kTile;
-        // S = Q K^T: n-tile nt covers keys 8 nt .. 8 nt + 7 of the tile
-        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int kk = 0; kk < C::kSteps; ++kk) {
-            const int key = 8 * (mi >> 1) + r8;
-            const int chunk = (kk & 3) * 2 + (mi & 1);
-            uint32_t b[4];
-            ldsm_x4(sk + (kk >> 2) * C::kSubBytes + key * 128 + ((chunk ^ (key & 7)) << 4), b);
-            mma_bf16_16816(sc[0], qa[kk], b[0], b[1]);
-            mma_bf16_16816(sc[1], qa[kk], b[2], b[3]);
-        }
-        // masks: rows below lo are not tokens; a key later than the row's query is not visible
-        float x[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int kt = 8 * nt + 2 * t4 + (e & 1);
-                const int pk = j * kBlock + kt - lo;
-                const int pq = (e < 2) ? pos_a : pos_b;
-                x[nt][e] = (kt >= lo && pk <= pq) ? sc[nt][e] * p.scale_log2 : -INFINITY;
-            }
-        float mx_a = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-        float mx_b = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-#pragma unroll
-        for (int o2 = 1; o2 < 4; o2 <<= 1) {
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, o2));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, o2));
-        }
-        const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-        const float ms_a = mn_a == -INFINITY ? 0.f : mn_a, ms_b = mn_b == -INFINITY ? 0.f : mn_b;
-        const float al_a = ex2_approx(m_a - ms_a), al_b = ex2_approx(m_b - ms_b);
-        m_a = mn_a;
-        m_b = mn_b;
-        uint32_t pa[4], pl[4];  // P (and its remainder) as the A operand of P V (k = the tile's 16 keys)
-        const bool split = j < kSplitBlocks;
-        float rs_a = 0.f, rs_b = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const float e0 = ex2_approx(x[nt][0] - ms_a), e1 = ex2_approx(x[nt][1] - ms_a);
-            const float e2 = ex2_approx(x[nt][2] - ms_b), e3 = ex2_approx(x[nt][3] - ms_b);
-            const __nv_bfloat162 ra = __floats2bfloat162_rn(e0, e1);
-            const __nv_bfloat162 rb = __floats2bfloat162_rn(e2, e3);
-            const float2 fa = __bfloat1622float2(ra), fb = __bfloat1622float2(rb);
-            rs_a += fa.x + fa.y;
-            rs_b += fb.x + fb.y;
-            pa[2 * nt + 0] = *reinterpret_cast<const uint32_t *>(&ra);
-            pa[2 * nt + 1] = *reinterpret_cast<const uint32_t *>(&rb);
-            if (split) {
-                const __nv_bfloat162 la = __floats2bfloat162_rn(e0 - fa.x, e1 - fa.y);
-                const __nv_bfloat162 lb = __floats2bfloat162_rn(e2 - fb.x, e3 - fb.y);
-                const float2 ga = __bfloat1622float2(la), gb = __bfloat1622float2(lb);
-                rs_a += ga.x + ga.y;
-                rs_b += gb.x + gb.y;
-                pl[2 * nt + 0] = *reinterpret_cast<const uint32_t *>(&la);
-                pl[2 * nt + 1] = *reinterpret_cast<const uint32_t *>(&lb);
-            }
-        }
-        l_a = l_a * al_a + rs_a;
-        l_b = l_b * al_b + rs_b;
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            o[i][0] *= al_a;
-            o[i][1] *= al_a;
-            o[i][2] *= al_b;
-            o[i][3] *= al_b;
-        }
-        // O += P V: n-tile i covers head-dim 8 i .. 8 i + 7
-#pragma unroll
-        for (int c = 0; c < D / 8; c += 2) {
-            const int key = 8 * (mi & 1) + r8;
-            const int chunk = (c & 7) + (mi >> 1);
-            uint32_t b[4];
-            ldsm_x4_trans(sv + (c >> 3) * C::kSubBytes + key * 128 + ((chunk ^ (key & 7)) << 4), b);
-            mma_bf16_16816(o[c], pa, b[0], b[1]);
-            mma_bf16_16816(o[c + 1], pa, b[2], b[3]);
-            if (split) {
-                mma_bf16_16816(o[c], pl, b[0], b[1]);
-                mma_bf16_16816(o[c + 1], pl, b[2], b[3]);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-    }
-    // ---- rows' sums over their 4 lanes, then the output ----
-#pragma unroll
-    for (int o2 = 1; o2 < 4; o2 <<= 1) {
-        l_a += __shfl_xor_sync(0xffffffffu, l_a, o2);
-        l_b += __shfl_xor_sync(0xffffffffu, l_b, o2);
-    }
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
-    auto out_row = [&](int r) -> __nv_bfloat16 * {
-        const int t = t0 + r / g;
-        return out + ((size_t)(q0 + t) * p.num_q_heads + h * g + r % g) * D;
-    };
-    const float ia = l_a > 0.f ? 1.f / l_a : 0.f, ib = l_b > 0.f ? 1.f / l_b : 0.f;
-    if (pos_a >= 0) {
-        __nv_bfloat16 *ra = out_row(r_lo + gq);
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i)
-            *reinterpret_cast<__nv_bfloat162 *>(ra + 8 * i + 2 * t4) = __floats2bfloat162_rn(o[i][0] * ia, o[i][1] * ia);
-    }
-    if (pos_b >= 0) {
-        __nv_bfloat16 *rb = out_row(r_lo + gq + 8);
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i)
-            *reinterpret_cast<__nv_bfloat162 *>(rb + 8 * i + 2 * t4) = __floats2bfloat162_rn(o[i][2] * ib, o[i][3] * ib);
-    }
-}
 
 // =====================================================================================
 // K1 (fp32): same decomposition on the CUDA cores, for fp32 caches where the

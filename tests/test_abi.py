@@ -94,15 +94,15 @@ def test_decode_rejects_bad_arguments_before_any_cuda_call(lib):
 
 def _prefill(lib, **kw):
     args = dict(out=1 << 12, q=1 << 12, k=1 << 12, v=1 << 12, bt=1 << 12, cl=1 << 12, qs=1 << 12, scale=0.1, hkv=8,
-                S=4, hq=8, d=64, maxb=4, nb=32, maxq=16, maxlen=64, dtype=1, stream=None)
+                S=4, hq=8, d=64, maxb=4, nb=32, T=40, maxq=16, maxlen=64, dtype=1, stream=None)
     args.update(kw)
     f = lib.paged_prefill_attention
     f.restype = ctypes.c_int
     vp = ctypes.c_void_p
-    f.argtypes = [vp] * 7 + [ctypes.c_float] + [ctypes.c_int] * 9 + [vp]
+    f.argtypes = [vp] * 7 + [ctypes.c_float] + [ctypes.c_int] * 10 + [vp]
     return f(args["out"], args["q"], args["k"], args["v"], args["bt"], args["cl"], args["qs"], args["scale"],
-             args["hkv"], args["S"], args["hq"], args["d"], args["maxb"], args["nb"], args["maxq"], args["maxlen"],
-             args["dtype"], args["stream"])
+             args["hkv"], args["S"], args["hq"], args["d"], args["maxb"], args["nb"], args["T"], args["maxq"],
+             args["maxlen"], args["dtype"], args["stream"])
 
 
 def test_prefill_rejects_bad_arguments_before_any_cuda_call(lib):
@@ -116,6 +116,7 @@ def test_prefill_rejects_bad_arguments_before_any_cuda_call(lib):
     assert _prefill(lib, scale=float("inf")) == -1
     assert _prefill(lib, S=0) == 0
     assert _prefill(lib, maxq=0) == 0                # no new tokens: nothing to do
+    assert _prefill(lib, T=-1) == -1
 
 
 def test_append_and_copy_reject_bad_arguments(lib):
