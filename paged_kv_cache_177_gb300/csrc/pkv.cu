@@ -189,6 +189,12 @@ int launch_prefill_tc(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUte
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     if (configured_device != dev) {
+        // the kernel's register split needs the launch count it was designed for; a build
+        // that got fewer registers per thread would wait forever in setmaxnreg.inc
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return PKV_ERR_CUDA;
+        if (fa.numRegs * C::kThreads < 128 * C::kLowRegs + C::kTiles * 128 * C::kHighRegs)
+            return PKV_ERR_UNSUPPORTED;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured_device = dev;

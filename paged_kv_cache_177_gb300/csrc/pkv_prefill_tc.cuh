@@ -22,7 +22,9 @@
 //                        O_t += P_t V_j with P_t read from tensor memory; the
 //                        next S_t follows right after. While one tile's
 //                        softmax runs, the tensor cores work on the other.
-//   warps 2-5, 6-9       softmax of tile 0 / tile 1, one thread per query row
+//   warps 2-3            idle (they complete warpgroup 0, which hands its
+//                        registers to the softmax warpgroups)
+//   warps 4-7, 8-11      softmax of tile 0 / tile 1, one thread per query row
 //                        (tensor-memory lane = row): the row max of S_t, a
 //                        rescale of its row of O_t when the max moved, then
 //                        P_t = 2^(S_t - max) written over S_t. At the end
@@ -69,7 +71,13 @@ struct TcCfg {
     static constexpr int kBarOff = kVOff + kStages * kStage;
     static constexpr int kSmem = kBarOff + 256 + 1024;     // + barriers, + 1024-byte alignment slack
     static constexpr int kSoftmaxWarps = 4 * kTiles;
-    static constexpr int kThreads = (2 + kSoftmaxWarps) * 32;
+    static constexpr int kThreads = (4 + kSoftmaxWarps) * 32;  // warpgroup 0: TMA, MMA, 2 idle warps
+    // register split (setmaxnreg): launched at kLaunchRegs each, warpgroup 0 gives
+    // registers to the softmax warpgroups
+    static constexpr int kLaunchRegs = 168;
+    static constexpr int kLowRegs = 72;
+    static constexpr int kHighRegs = 208;
+    static_assert(128 * kLowRegs + kTiles * 128 * kHighRegs <= kThreads * kLaunchRegs, "register split");
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kTileCols = 256;             // per tile: S / P at +0, O at +128
     static constexpr uint32_t kOCol = 128;
@@ -150,7 +158,9 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
     const uint32_t q_s = smem_u32(base + C::kQOff), k_s = smem_u32(base + C::kKOff);
     const uint32_t v_s = smem_u32(base + C::kVOff);
 
-    if (warp == 0) {
+    if (warp < 4) {
+      setmaxnreg_dec<C::kLowRegs>();
+      if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             bool ok = true;
@@ -168,33 +178,34 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
             int issued_k = 0, issued_v = 0;  // chunks whose K / V copies were issued
             for (int j = 0; j < nc_all && ok; ++j) {
                 const int st = j & 1;
-                int z[C::kChunkBlocks], y[C::kChunkBlocks];
-#pragma unroll
-                for (int bi = 0; bi < C::kChunkBlocks; ++bi) {
+                if (j >= 2 && !mbar_wait(&b.k_empty[st], ((j - 2) >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                // block bi of the chunk: tile row z of the cache view (-1: past the sequence or a bad
+                // id, outside the tensor, reads as zeros), first slot y
+                auto where = [&](int bi, int &z, int &y) {
                     const int blk = j * C::kChunkBlocks + bi;
-                    z[bi] = -1;  // past the sequence (or a bad id): outside the tensor, reads as zeros
-                    y[bi] = 0;
+                    z = -1;
+                    y = 0;
                     if (blk < nblk) {
                         const int pb = __ldg(table + blk);
                         if (pb < 0 || pb >= p.num_blocks)
                             raise_error(PKV_DEVERR_BLOCK_ID);
                         else
-                            z[bi] = pb * p.num_kv_heads + h;
-                        if (blk == nblk - 1) y[bi] = last_valid - kBlock;
+                            z = pb * p.num_kv_heads + h;
+                        if (blk == nblk - 1) y = last_valid - kBlock;
                     }
-                }
-                if (j >= 2 && !mbar_wait(&b.k_empty[st], ((j - 2) >> 1) & 1)) {
-                    ok = false;
-                    break;
-                }
+                };
                 // K chunk as [half][128 keys][64]: 8-row groups 1024 bytes apart along the keys
                 mbar_arrive_expect_tx(&b.k_full[st], C::kStage);
-#pragma unroll
-                for (int bi = 0; bi < C::kChunkBlocks; ++bi)
-#pragma unroll
+                for (int bi = 0; bi < C::kChunkBlocks; ++bi) {
+                    int z, y;
+                    where(bi, z, y);
                     for (int u = 0; u < C::kHalves; ++u)
                         tma_load_4d(base + C::kKOff + st * C::kStage + u * C::kHalfRows + bi * (kBlock * 128), &tmk,
-                                    0, y[bi], u, z[bi], &b.k_full[st]);
+                                    0, y, u, z, &b.k_full[st]);
+                }
                 issued_k = j + 1;
                 if (j >= 2 && !mbar_wait(&b.v_empty[st], ((j - 2) >> 1) & 1)) {
                     ok = false;
@@ -202,12 +213,13 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                 }
                 // V chunk as [block][half][16 keys][64]
                 mbar_arrive_expect_tx(&b.v_full[st], C::kStage);
-#pragma unroll
-                for (int bi = 0; bi < C::kChunkBlocks; ++bi)
-#pragma unroll
+                for (int bi = 0; bi < C::kChunkBlocks; ++bi) {
+                    int z, y;
+                    where(bi, z, y);
                     for (int u = 0; u < C::kHalves; ++u)
                         tma_load_4d(base + C::kVOff + st * C::kStage + bi * C::kBlockBytes + u * (kBlock * 128),
-                                    &tmv, 0, y[bi], u, z[bi], &b.v_full[st]);
+                                    &tmv, 0, y, u, z, &b.v_full[st]);
+                }
                 issued_v = j + 1;
             }
             if (!ok) raise_error(PKV_DEVERR_TIMEOUT);
@@ -278,9 +290,11 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
             mbar_wait(&b.drain, 0);
         }
         __syncwarp();
+      }
     } else {
+        setmaxnreg_inc<C::kHighRegs>();
         // ------------------------------ softmax ------------------------------
-        const int t = (warp - 2) >> 2;  // query tile
+        const int t = (warp - 4) >> 2;  // query tile
         const int quad = warp & 3;       // tensor-memory lanes 32 quad .. 32 quad + 31
         const int row = quad * 32 + lane;
         static_assert(C::kTiles == 2, "tile selection below");
@@ -293,47 +307,54 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
         const int tile_first = first_pos + tok0;  // the smallest query position of the tile
         float m = -INFINITY, l = 0.f;
         bool ok = true;
-        // scores of keys c0 .. c0 + 31 of chunk j in the log2 domain, keys this row does not see at -inf
-        auto scale_mask = [&](float (&v)[32], int j, int c0, bool plain) {
+        // Scores are kept raw (unscaled): with sl = |scale log2 e| and the sign folded into the scores,
+        // x * sl is the log2-domain score, and the max of x gives the max of x * sl.
+        const float sl = fabsf(p.scale_log2);
+        const float sgn = p.scale_log2 < 0.f ? -1.f : 1.f;
+        // keys c0 .. c0 + 31 of chunk j this row does not see -> -inf
+        auto mask = [&](float (&v)[32], int j, int c0) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] *= p.scale_log2;
-            if (!plain) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int kc = c0 + e;
-                    const int blk = j * C::kChunkBlocks + kc / kBlock, r = kc % kBlock;
-                    const int lo = blk == nblk - 1 ? kBlock - last_valid : 0;
-                    const bool vis = blk < nblk && r >= lo && blk * kBlock + r - lo <= pos;
-                    v[e] = vis ? v[e] : -INFINITY;
-                }
+            for (int e = 0; e < 32; ++e) {
+                const int kc = c0 + e;
+                const int blk = j * C::kChunkBlocks + kc / kBlock, r = kc % kBlock;
+                const int lo = blk == nblk - 1 ? kBlock - last_valid : 0;
+                const bool vis = blk < nblk && r >= lo && blk * kBlock + r - lo <= pos;
+                v[e] = vis ? v[e] : -INFINITY;
             }
         };
         for (int j = 0; j < ncs; ++j) {
             if (!(ok = warp_wait(&b.s_full[t], j & 1))) break;
             tc_fence_after();
+            // the whole row of S_t in registers (one tensor-memory round trip)
+            float x[4][32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32(cols + q * 32, x[q]);
+            tmem_wait_ld();
+            if (sgn < 0.f) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[q][e] = -x[q][e];
+            }
             // only chunks holding the end of the sequence, or keys past the tile's first query, need masks
             const bool plain = (j + 1) * C::kChunkBlocks < nblk && (j + 1) * C::kKeys - 1 <= tile_first;
-            // pass 1: the row max
+            if (!plain) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) mask(x[q], j, q * 32);
+            }
             float mx = -INFINITY;
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float a[32], c[32];
-                tmem_ld32(cols + hf * 64, a);
-                tmem_ld32(cols + hf * 64 + 32, c);
-                tmem_wait_ld();
-                scale_mask(a, j, hf * 64, plain);
-                scale_mask(c, j, hf * 64 + 32, plain);
+            for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fmaxf(a[e], c[e]));
-            }
-            const float m_new = fmaxf(m, mx);
+                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, x[q][e]);
+            const float m_new = fmaxf(m, mx * sl);
             const bool move = m_new > m + 8.f;
             const float m_use = move ? m_new : m;
             const float ms = m_use == -INFINITY ? 0.f : m_use;
             const float alpha = ex2_approx(m - ms);
             // this tile's O is quiescent here (P V of the previous chunk ran before S of this one)
             if (j > 0 && __any_sync(0xffffffffu, move && m != -INFINITY)) {
-#pragma unroll
+#pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     float o[32];
                     tmem_ld32(cols + C::kOCol + c * 32, o);
@@ -344,36 +365,29 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                 }
             }
             m = m_use;
-            // pass 2: P = 2^(x - reference max) in bf16 over each quarter's own score columns:
-            // keys 32 q + 2 i, + 1 at column 32 q + i, their rounding remainders at + 16
+            // P = 2^(x sl - reference max) in bf16 over each quarter's own score columns:
+            // keys 32 q + 2 i, + 1 at column 32 q + i, their rounding remainders at + 16.
+            // The row sum takes the unrounded weights: the first chunk's P (hi + lo) matches
+            // them to 2^-16, later chunks' rounding errors average out over the keys.
             float rs = 0.f;
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float a[2][32];
-                tmem_ld32(cols + hf * 64, a[0]);
-                tmem_ld32(cols + hf * 64 + 32, a[1]);
-                tmem_wait_ld();
+            for (int q = 0; q < 4; ++q) {
+                uint32_t hi[16], lo[16];
 #pragma unroll
-                for (int qq = 0; qq < 2; ++qq) {
-                    scale_mask(a[qq], j, hf * 64 + qq * 32, plain);
-                    uint32_t hi[16], lo[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float e0 = ex2_approx(a[qq][2 * i] - ms), e1 = ex2_approx(a[qq][2 * i + 1] - ms);
-                        const __nv_bfloat162 ph = __floats2bfloat162_rn(e0, e1);
+                for (int i = 0; i < 16; ++i) {
+                    const float e0 = ex2_approx(fmaf(x[q][2 * i], sl, -ms));
+                    const float e1 = ex2_approx(fmaf(x[q][2 * i + 1], sl, -ms));
+                    rs += e0 + e1;
+                    const __nv_bfloat162 ph = __floats2bfloat162_rn(e0, e1);
+                    hi[i] = *reinterpret_cast<const uint32_t *>(&ph);
+                    if (j == 0) {
                         const float2 fh = __bfloat1622float2(ph);
-                        rs += fh.x + fh.y;
-                        hi[i] = *reinterpret_cast<const uint32_t *>(&ph);
-                        if (j == 0) {
-                            const __nv_bfloat162 pl = __floats2bfloat162_rn(e0 - fh.x, e1 - fh.y);
-                            const float2 fl = __bfloat1622float2(pl);
-                            rs += fl.x + fl.y;
-                            lo[i] = *reinterpret_cast<const uint32_t *>(&pl);
-                        }
+                        const __nv_bfloat162 pl = __floats2bfloat162_rn(e0 - fh.x, e1 - fh.y);
+                        lo[i] = *reinterpret_cast<const uint32_t *>(&pl);
                     }
-                    tmem_st16(cols + hf * 64 + qq * 32, hi);
-                    if (j == 0) tmem_st16(cols + hf * 64 + qq * 32 + 16, lo);
                 }
+                tmem_st16(cols + q * 32, hi);
+                if (j == 0) tmem_st16(cols + q * 32 + 16, lo);
             }
             tmem_wait_st();
             l = l * alpha + rs;
