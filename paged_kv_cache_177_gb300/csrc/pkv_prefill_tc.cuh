@@ -182,30 +182,36 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                     ok = false;
                     break;
                 }
-                // block bi of the chunk: tile row z of the cache view (-1: past the sequence or a bad
-                // id, outside the tensor, reads as zeros), first slot y
-                auto where = [&](int bi, int &z, int &y) {
+                // the chunk's blocks: tile row z of the cache view (-1: past the sequence or a bad
+                // id, outside the tensor, reads as zeros) and first slot y; the table entries are
+                // loaded together so their latencies overlap
+                int z[C::kChunkBlocks], y[C::kChunkBlocks];
+#pragma unroll
+                for (int bi = 0; bi < C::kChunkBlocks; ++bi) {
                     const int blk = j * C::kChunkBlocks + bi;
-                    z = -1;
-                    y = 0;
+                    z[bi] = blk < nblk ? __ldg(table + blk) : -1;
+                }
+#pragma unroll
+                for (int bi = 0; bi < C::kChunkBlocks; ++bi) {
+                    const int blk = j * C::kChunkBlocks + bi;
+                    y[bi] = blk == nblk - 1 ? last_valid - kBlock : 0;
                     if (blk < nblk) {
-                        const int pb = __ldg(table + blk);
-                        if (pb < 0 || pb >= p.num_blocks)
+                        if (z[bi] < 0 || z[bi] >= p.num_blocks) {
                             raise_error(PKV_DEVERR_BLOCK_ID);
-                        else
-                            z = pb * p.num_kv_heads + h;
-                        if (blk == nblk - 1) y = last_valid - kBlock;
+                            z[bi] = -1;
+                        } else {
+                            z[bi] = z[bi] * p.num_kv_heads + h;
+                        }
                     }
-                };
+                }
                 // K chunk as [half][128 keys][64]: 8-row groups 1024 bytes apart along the keys
                 mbar_arrive_expect_tx(&b.k_full[st], C::kStage);
-                for (int bi = 0; bi < C::kChunkBlocks; ++bi) {
-                    int z, y;
-                    where(bi, z, y);
+#pragma unroll
+                for (int bi = 0; bi < C::kChunkBlocks; ++bi)
+#pragma unroll
                     for (int u = 0; u < C::kHalves; ++u)
                         tma_load_4d(base + C::kKOff + st * C::kStage + u * C::kHalfRows + bi * (kBlock * 128), &tmk,
-                                    0, y, u, z, &b.k_full[st]);
-                }
+                                    0, y[bi], u, z[bi], &b.k_full[st]);
                 issued_k = j + 1;
                 if (j >= 2 && !mbar_wait(&b.v_empty[st], ((j - 2) >> 1) & 1)) {
                     ok = false;
@@ -213,13 +219,12 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                 }
                 // V chunk as [block][half][16 keys][64]
                 mbar_arrive_expect_tx(&b.v_full[st], C::kStage);
-                for (int bi = 0; bi < C::kChunkBlocks; ++bi) {
-                    int z, y;
-                    where(bi, z, y);
+#pragma unroll
+                for (int bi = 0; bi < C::kChunkBlocks; ++bi)
+#pragma unroll
                     for (int u = 0; u < C::kHalves; ++u)
                         tma_load_4d(base + C::kVOff + st * C::kStage + bi * C::kBlockBytes + u * (kBlock * 128),
-                                    &tmv, 0, y, u, z, &b.v_full[st]);
-                }
+                                    &tmv, 0, y[bi], u, z[bi], &b.v_full[st]);
                 issued_v = j + 1;
             }
             if (!ok) raise_error(PKV_DEVERR_TIMEOUT);
@@ -342,11 +347,15 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) mask(x[q], j, q * 32);
             }
-            float mx = -INFINITY;
+            float mxs[8];  // independent partial maxima (a single chain would be 128 dependent steps)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mxs[i] = -INFINITY;
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, x[q][e]);
+                for (int e = 0; e < 32; ++e) mxs[e & 7] = fmaxf(mxs[e & 7], x[q][e]);
+            const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                                   fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
             const float m_new = fmaxf(m, mx * sl);
             const bool move = m_new > m + 8.f;
             const float m_use = move ? m_new : m;
@@ -369,7 +378,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
             // keys 32 q + 2 i, + 1 at column 32 q + i, their rounding remainders at + 16.
             // The row sum takes the unrounded weights: the first chunk's P (hi + lo) matches
             // them to 2^-16, later chunks' rounding errors average out over the keys.
-            float rs = 0.f;
+            float rss[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t hi[16], lo[16];
@@ -377,7 +386,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                 for (int i = 0; i < 16; ++i) {
                     const float e0 = ex2_approx(fmaf(x[q][2 * i], sl, -ms));
                     const float e1 = ex2_approx(fmaf(x[q][2 * i + 1], sl, -ms));
-                    rs += e0 + e1;
+                    rss[i & 7] += e0 + e1;
                     const __nv_bfloat162 ph = __floats2bfloat162_rn(e0, e1);
                     hi[i] = *reinterpret_cast<const uint32_t *>(&ph);
                     if (j == 0) {
@@ -390,6 +399,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                 if (j == 0) tmem_st16(cols + q * 32 + 16, lo);
             }
             tmem_wait_st();
+            const float rs = ((rss[0] + rss[1]) + (rss[2] + rss[3])) + ((rss[4] + rss[5]) + (rss[6] + rss[7]));
             l = l * alpha + rs;
             tc_fence_before();
             __syncwarp();
