@@ -1,0 +1,20 @@
+"""bench.py reports a kernel's DRAM traffic from a committed ncu summary only
+while the kernel sources are the ones the summary was captured from."""
+import bench
+
+
+def test_traffic_comes_from_the_matching_summary():
+    t, src = bench.profiled_traffic("mha13b", "decode_bf16_persistent_kernel")
+    assert src == "profiles/decode_bf16_persistent_kernel_mha13b.md"
+    assert t is None or t > 600_000_000     # null only after a kernel change
+
+
+def test_traffic_is_null_once_the_sources_change(monkeypatch):
+    monkeypatch.setattr(bench, "kernel_sources_sha256", lambda: "0" * 64)
+    t, why = bench.profiled_traffic("mha13b", "decode_bf16_persistent_kernel")
+    assert t is None and "changed" in why
+
+
+def test_traffic_is_null_without_a_capture():
+    t, why = bench.profiled_traffic("gqa8b", "decode_bf16_persistent_kernel")
+    assert t is None and "no ncu capture" in why
