@@ -39,10 +39,12 @@
 // and the weights 2^(x - reference) stay below 2^8. Softmax is invariant to
 // the reference, so the result is the same.
 //
-// Weights of the first chunk also enter P V as their bf16 rounding remainder
-// (a second P V product), as the mma.sync kernels do for positions < 64: rows
-// that see only a few keys would otherwise carry the full bf16 rounding of
-// their weights.
+// The weights of the first chunk also enter P V as their bf16 rounding
+// remainder (a second P V product), as the mma.sync kernels do for positions
+// < 64: rows that see only a few keys would otherwise carry the full bf16
+// rounding of their weights. (Limiting it to tiles that hold such rows was
+// measured slower: the extra first-chunk work staggers the two tiles'
+// softmax phases, which then overlap the other tile's MMAs better.)
 //
 // Every wait is bounded; on a timeout the CTA records PKV_DEVERR_TIMEOUT,
 // waits (bounded) for its in-flight copies and MMAs, frees its tensor memory
@@ -247,6 +249,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                 }
             };
             auto issue_pv = [&](int t, int j) {
+                const bool split = j == 0;  // the first chunk's weights carry their rounding remainder
 #pragma unroll
                 for (int kk = 0; kk < C::kChunkBlocks; ++kk) {  // 16 keys (one block) per step
                     const uint64_t vd =
@@ -254,7 +257,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                     // P of keys 16 kk .. 16 kk + 15: columns 32 (kk / 2) + 8 (kk % 2); remainder 16 further
                     const uint32_t pa = tmem + t * C::kTileCols + (kk >> 1) * 32 + (kk & 1) * 8;
                     umma_bf16_tmem_a(tmem + t * C::kTileCols + C::kOCol, pa, vd, idesc_o, j > 0 || kk > 0);
-                    if (j == 0) umma_bf16_tmem_a(tmem + t * C::kTileCols + C::kOCol, pa + 16, vd, idesc_o, true);
+                    if (split) umma_bf16_tmem_a(tmem + t * C::kTileCols + C::kOCol, pa + 16, vd, idesc_o, true);
                 }
             };
             bool ok = mbar_wait(&b.q_full, 0) && mbar_wait(&b.k_full[0], 0);
@@ -316,15 +319,30 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
         // x * sl is the log2-domain score, and the max of x gives the max of x * sl.
         const float sl = fabsf(p.scale_log2);
         const float sgn = p.scale_log2 < 0.f ? -1.f : 1.f;
-        // keys c0 .. c0 + 31 of chunk j this row does not see -> -inf
-        auto mask = [&](float (&v)[32], int j, int c0) {
+        // Keys of chunk j this row does not see -> -inf. Column kc of a full block holds position
+        // 128 j + kc; in the chunk holding the sequence's last block (index lb in the chunk, loaded
+        // lo rows early) column kc >= 16 lb holds position 128 j + kc - lo and is a token only
+        // from 16 lb + lo on; columns past that block are zeros. So a row at position pos sees
+        // columns 0 .. min(P, 16 lb - 1) and 16 lb + lo .. min(P + lo, 16 lb + 15), P = pos - 128 j.
+        auto mask = [&](float (&v)[4][32], int j) {
+            const int P = pos - j * C::kKeys;
+            const int lb = nblk - 1 - j * C::kChunkBlocks;
+            if (lb >= C::kChunkBlocks) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int kc = c0 + e;
-                const int blk = j * C::kChunkBlocks + kc / kBlock, r = kc % kBlock;
-                const int lo = blk == nblk - 1 ? kBlock - last_valid : 0;
-                const bool vis = blk < nblk && r >= lo && blk * kBlock + r - lo <= pos;
-                v[e] = vis ? v[e] : -INFINITY;
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[q][e] = q * 32 + e <= P ? v[q][e] : -INFINITY;
+            } else {
+                const int lo = kBlock - last_valid;
+                const int a_end = min(P, lb * kBlock - 1);
+                const int b_lo = lb * kBlock + lo, b_hi = min(P + lo, lb * kBlock + kBlock - 1);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int kc = q * 32 + e;
+                        v[q][e] = (kc <= a_end || (kc >= b_lo && kc <= b_hi)) ? v[q][e] : -INFINITY;
+                    }
             }
         };
         for (int j = 0; j < ncs; ++j) {
@@ -343,10 +361,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
             }
             // only chunks holding the end of the sequence, or keys past the tile's first query, need masks
             const bool plain = (j + 1) * C::kChunkBlocks < nblk && (j + 1) * C::kKeys - 1 <= tile_first;
-            if (!plain) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) mask(x[q], j, q * 32);
-            }
+            if (!plain) mask(x, j);
             float mxs[8];  // independent partial maxima (a single chain would be 128 dependent steps)
 #pragma unroll
             for (int i = 0; i < 8; ++i) mxs[i] = -INFINITY;
@@ -378,6 +393,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
             // keys 32 q + 2 i, + 1 at column 32 q + i, their rounding remainders at + 16.
             // The row sum takes the unrounded weights: the first chunk's P (hi + lo) matches
             // them to 2^-16, later chunks' rounding errors average out over the keys.
+            const bool split = j == 0;
             float rss[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -389,14 +405,14 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                     rss[i & 7] += e0 + e1;
                     const __nv_bfloat162 ph = __floats2bfloat162_rn(e0, e1);
                     hi[i] = *reinterpret_cast<const uint32_t *>(&ph);
-                    if (j == 0) {
+                    if (split) {
                         const float2 fh = __bfloat1622float2(ph);
                         const __nv_bfloat162 pl = __floats2bfloat162_rn(e0 - fh.x, e1 - fh.y);
                         lo[i] = *reinterpret_cast<const uint32_t *>(&pl);
                     }
                 }
                 tmem_st16(cols + q * 32, hi);
-                if (j == 0) tmem_st16(cols + q * 32 + 16, lo);
+                if (split) tmem_st16(cols + q * 32 + 16, lo);
             }
             tmem_wait_st();
             const float rs = ((rss[0] + rss[1]) + (rss[2] + rss[3])) + ((rss[4] + rss[5]) + (rss[6] + rss[7]));
