@@ -215,13 +215,13 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
-def oracle_sample(lay: W.Layout, host: dict, target_s: float):
+def oracle_sample(lay: W.Layout, host: dict, target_s: float, nthreads: int = 0):
     """Times the oracle (fp64, all host cores) on a bounded sample of the
     workload -- about ``target_s`` seconds of CPU work -- after applying the
     step's copies and appends on the host.  The sample grows by sequences
     until one pass takes a quarter of the budget (or covers the workload),
-    then passes repeat until the budget is spent.  Returns
-    (GB/s, seconds, sequences, passes, sample bytes per pass)."""
+    then passes repeat until the budget is spent.  ``nthreads`` = 0 uses every
+    host core.  Returns (GB/s, seconds, sequences, passes, sample bytes per pass)."""
     import oracle
 
     eb = 2 if lay.spec.dtype == "bf16" else 4
@@ -234,10 +234,10 @@ def oracle_sample(lay: W.Layout, host: dict, target_s: float):
         t0 = time.perf_counter()
         oracle.paged_decode_attention(host["q"], host["k_cache"], host["v_cache"], lay.block_tables,
                                       lay.context_lens, 1.0 / math.sqrt(lay.spec.head_dim), lay.spec.num_kv_heads,
-                                      seq_ids=ids, nthreads=cpu_cores())
+                                      seq_ids=ids, nthreads=nthreads or cpu_cores())
         return time.perf_counter() - t0
 
-    n = min(len(order), max(1, cpu_cores() // max(1, lay.spec.num_kv_heads)))
+    n = min(len(order), max(1, (nthreads or cpu_cores()) // max(1, lay.spec.num_kv_heads)))
     dt = run(order[:n])
     while dt < target_s / 4 and n < len(order):
         n = min(len(order), max(n + 1, int(n * min(8.0, target_s / 4 / max(dt, 1e-4)))))
@@ -472,6 +472,9 @@ def run_ours(args, rank, world, local, dist):
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{nseq} of {S} sequences ({sb / 1e6:.1f} MB of K/V, all heads) x {passes} passes in "
                          f"{secs:.1f} s, fp64 C oracle, after the step's copies and appends"}
+        g1, s1, n1, p1, b1 = oracle_sample(lay, host, min(3.0, args.cpu_seconds / 3), nthreads=1)
+        cpu["single_thread"] = {"value": round(g1, 4), "unit": "GB/s", "cores": 1,
+                                "sample": f"{n1} sequences ({b1 / 1e6:.1f} MB) x {p1} passes in {s1:.1f} s"}
     srt = sorted(step_ms)
     roof_kernel = "decode_bf16_persistent_kernel" if persistent else "decode_bf16_kernel"
     # the captures were taken on the workloads' default launch configuration
