@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) mxs[e & 7] = fmaxf(mxs[e & 7], x[q][e]);
+                for (int e = 0; e < 32; e += 2) mxs[(e >> 1) & 7] = max3f(mxs[(e >> 1) & 7], x[q][e], x[q][e + 1]);
             const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
                                    fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
             const float m_new = fmaxf(m, mx * sl);
@@ -394,15 +394,19 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
             // The row sum takes the unrounded weights: the first chunk's P (hi + lo) matches
             // them to 2^-16, later chunks' rounding errors average out over the keys.
             const bool split = j == 0;
-            float rss[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
+            const uint64_t sl2 = pack_f2(sl, sl), nms2 = pack_f2(-ms, -ms);
+            uint64_t rss[4];  // independent partial sums, two lanes each
+#pragma unroll
+            for (int i = 0; i < 4; ++i) rss[i] = pack_f2(0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float e0 = ex2_approx(fmaf(x[q][2 * i], sl, -ms));
-                    const float e1 = ex2_approx(fmaf(x[q][2 * i + 1], sl, -ms));
-                    rss[i & 7] += e0 + e1;
+                    float a0, a1;
+                    unpack_f2(fma_f2(pack_f2(x[q][2 * i], x[q][2 * i + 1]), sl2, nms2), a0, a1);
+                    const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+                    rss[i & 3] = add_f2(rss[i & 3], pack_f2(e0, e1));
                     const __nv_bfloat162 ph = __floats2bfloat162_rn(e0, e1);
                     hi[i] = *reinterpret_cast<const uint32_t *>(&ph);
                     if (split) {
@@ -415,7 +419,13 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                 if (split) tmem_st16(cols + q * 32 + 16, lo);
             }
             tmem_wait_st();
-            const float rs = ((rss[0] + rss[1]) + (rss[2] + rss[3])) + ((rss[4] + rss[5]) + (rss[6] + rss[7]));
+            float rs;
+            {
+                float r[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) unpack_f2(rss[i], r[2 * i], r[2 * i + 1]);
+                rs = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
+            }
             l = l * alpha + rs;
             tc_fence_before();
             __syncwarp();
