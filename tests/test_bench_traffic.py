@@ -5,8 +5,18 @@ import bench
 
 def test_traffic_comes_from_the_matching_summary():
     t, src = bench.profiled_traffic("mha13b", "decode_bf16_persistent_kernel")
-    assert src == "profiles/decode_bf16_persistent_kernel_mha13b.md"
-    assert t is None or t > 600_000_000     # null only after a kernel change
+    if t is None:                           # the kernel sources changed since the capture
+        assert "changed since profiles/decode_bf16_persistent_kernel_mha13b.md" in src
+    else:
+        assert src == "profiles/decode_bf16_persistent_kernel_mha13b.md" and t > 600_000_000
+
+
+def test_traffic_follows_the_recorded_fingerprint(monkeypatch):
+    with open(bench.os.path.join(bench.ROOT, "profiles", "decode_bf16_persistent_kernel_mha13b.md")) as f:
+        sha = [ln.split(": ", 1)[1].strip() for ln in f if ln.startswith("source_sha256: ")][0]
+    monkeypatch.setattr(bench, "kernel_sources_sha256", lambda: sha)
+    t, src = bench.profiled_traffic("mha13b", "decode_bf16_persistent_kernel")
+    assert src == "profiles/decode_bf16_persistent_kernel_mha13b.md" and t > 600_000_000
 
 
 def test_traffic_is_null_once_the_sources_change(monkeypatch):
