@@ -137,6 +137,10 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
  *   pkv_decode_workspace_bytes(...) bytes, zero-filled before its first use
  *   (may be NULL when that size is 0). Concurrent calls must not share a
  *   workspace. After a call that raised PKV_DEVERR_TIMEOUT, zero it again.
+ * q, out, block_tables and context_lens may point to page-locked host memory
+ *   (mapped into the device's address space, as cudaHostAlloc gives): the
+ *   kernels read and write them in place over the host link. The caches and
+ *   the workspace must be device memory.
  */
 int paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                            const int32_t *block_tables, const int32_t *context_lens, float scale,
@@ -220,6 +224,7 @@ int paged_prefill_attention(void *out, const void *q, const void *k_cache, const
  * Negative slots are skipped (padding). Slots >= num_blocks*16 are skipped
  * and flagged (PKV_DEVERR_SLOT). Two tokens with the same slot race.
  * slot_mapping: int64 [num_tokens]. Bit-exact copy.
+ * k, v and slot_mapping may point to page-locked host memory (read in place).
  */
 int kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache, void *v_cache,
               int num_tokens, int num_kv_heads, int head_dim, int num_blocks, pkv_dtype dtype, void *stream);
@@ -228,7 +233,7 @@ int kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k
  * Block copy (copy-on-write): for each pair i, copy physical block
  * src_dst_pairs[i][0] onto src_dst_pairs[i][1] -- all kv heads, all 16
  * slots -- in both k_cache and v_cache. src_dst_pairs: int64 [num_pairs][2],
- * device. Pairs must not overlap (all destinations distinct, no destination
+ * device or page-locked host memory. Pairs must not overlap (all destinations distinct, no destination
  * also a source): check them on the host with pkv_check_copy_pairs. Pairs out
  * of range are skipped and flagged (PKV_DEVERR_PAIR). Bit-exact copy.
  */

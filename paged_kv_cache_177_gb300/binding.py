@@ -102,6 +102,22 @@ def _dev(*ts: torch.Tensor) -> torch.device:
     return d
 
 
+def _dev_io(device_tensors, io_tensors) -> torch.device:
+    """Device of the calls whose per-step arguments may also sit in pinned
+    host memory: ``device_tensors`` (the caches, the workspace) must be on one
+    CUDA device; each of ``io_tensors`` on that device or pinned on the host,
+    where the kernels read or write it in place over the host link."""
+    d = _dev(*device_tensors)
+    for t in io_tensors:
+        if t is None or t.numel() == 0:      # nothing the kernels would touch
+            continue
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+        if t.device != d and not (t.device.type == "cpu" and t.is_pinned()):
+            raise ValueError("per-step arguments must be on the caches' device or in pinned host memory")
+    return d
+
+
 def _stream_ptr(device: torch.device, stream: Optional[torch.cuda.Stream]) -> int:
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return s.cuda_stream
@@ -135,7 +151,7 @@ def decode_args(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cac
                 stream: Optional[torch.cuda.Stream] = None) -> tuple:
     """Checks and marshals the arguments of one paged_decode_attention call
     (see there) into the C-ABI argument tuple, for ``decode_raw``."""
-    dev = _dev(out, q, k_cache, v_cache, block_tables, context_lens)
+    dev = _dev_io([k_cache, v_cache], [out, q, block_tables, context_lens])
     dt = _dtype_code(q)
     if not (out.dtype == q.dtype == k_cache.dtype == v_cache.dtype):
         raise TypeError("q, out and the caches must share one dtype")
@@ -154,8 +170,8 @@ def decode_args(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cac
     need = workspace_bytes(S, Hq, Hkv, D, max_context_len, partition_tokens)
     if need and workspace is None:
         workspace = torch.zeros(need, dtype=torch.uint8, device=dev)   # must start zero-filled
-    if workspace is not None:
-        _dev(workspace)
+    if workspace is not None and _dev(workspace) != dev:
+        raise ValueError("the workspace must be on the caches' device")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     # the tensors ride along so they outlive the raw pointers
     return ((_p(out), _p(q), _p(k_cache), _p(v_cache), _p(block_tables), _p(context_lens), float(scale), Hkv, S, Hq,
@@ -183,6 +199,8 @@ def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
     > 0 fixed partitions of that many tokens.
     A caller-provided ``workspace`` must have been zero-filled once before
     its first use; the library leaves it zero-filled after each call.
+    q, out, block_tables and context_lens may be pinned host tensors: the
+    kernels then read and write them in place (no separate copy).
     """
     decode_raw(decode_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
                            max_context_len=max_context_len, partition_tokens=partition_tokens, workspace=workspace,
@@ -288,8 +306,9 @@ def paged_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.T
 
 def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
               v_cache: torch.Tensor, *, stream: Optional[torch.cuda.Stream] = None) -> None:
-    """cache[slot // 16, :, slot % 16, :] = k[t] (and v) for each slot >= 0."""
-    dev = _dev(k, v, slot_mapping, k_cache, v_cache)
+    """cache[slot // 16, :, slot % 16, :] = k[t] (and v) for each slot >= 0.
+    k, v and slot_mapping may be pinned host tensors (read in place)."""
+    dev = _dev_io([k_cache, v_cache], [k, v, slot_mapping])
     dt = _dtype_code(k)
     if not (k.dtype == v.dtype == k_cache.dtype == v_cache.dtype):
         raise TypeError("k, v and the caches must share one dtype")
@@ -315,8 +334,9 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: tor
     """Copies whole blocks src -> dst of both caches.  ``src_dst_pairs``:
     int64 [n, 2] on the device.  With ``check`` the pairs are range- and
     overlap-checked on the host first (``host_pairs`` if given, else a copy
-    of the device pairs, which synchronises)."""
-    dev = _dev(k_cache, v_cache, src_dst_pairs)
+    of the device pairs, which synchronises).  The pairs may also be a
+    pinned host tensor (read in place)."""
+    dev = _dev_io([k_cache, v_cache], [src_dst_pairs])
     dt = _dtype_code(k_cache)
     if src_dst_pairs.dtype != torch.int64:
         raise TypeError("src_dst_pairs must be int64")

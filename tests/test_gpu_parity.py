@@ -298,3 +298,33 @@ def test_persistent_step_in_a_cuda_graph():
         g.replay()
         torch.cuda.synchronize()
         H.assert_close(out, ref, "bf16", "persistent graph replay")
+
+
+def test_per_step_arguments_in_pinned_host_memory():
+    """q, out, tables, lengths, new K/V, slots and copy pairs read and written
+    in place in pinned host memory give the same bits as device copies, on
+    the persistent and the split grid paths."""
+    b = H.lib()
+    for name, pt in (("gqa8b", -1), ("parallel_sampling", 128)):
+        w = W.make_workload(name, num_seqs=24, num_prompts=6, seed=77) if name == "parallel_sampling" else \
+            W.make_workload(name, lengths_list=tuple(range(1, 2000, 83)), seed=77)
+        lay = w.layout
+        wd = w.to("cuda")
+        pin = lambda t: t.contiguous().pin_memory()
+        kc2, vc2 = wd.k_cache.clone(), wd.v_cache.clone()
+        # device arguments
+        b.copy_blocks(wd.k_cache, wd.v_cache, wd.cow_pairs, host_pairs=lay.cow_pairs)
+        b.kv_append(wd.k_new, wd.v_new, wd.slot_mapping, wd.k_cache, wd.v_cache)
+        out_d = torch.empty_like(wd.q)
+        b.paged_decode_attention(out_d, wd.q, wd.k_cache, wd.v_cache, wd.block_tables, wd.context_lens, w.scale,
+                                 max_context_len=lay.max_context_len, partition_tokens=pt)
+        # the same step with the per-step arguments in pinned host memory
+        b.copy_blocks(kc2, vc2, pin(w.cow_pairs), host_pairs=lay.cow_pairs)
+        b.kv_append(pin(w.k_new), pin(w.v_new), pin(w.slot_mapping), kc2, vc2)
+        out_h = torch.full(tuple(w.q.shape), float("nan"), dtype=w.q.dtype).pin_memory()
+        b.paged_decode_attention(out_h, pin(w.q), kc2, vc2, pin(w.block_tables), pin(w.context_lens), w.scale,
+                                 max_context_len=lay.max_context_len, partition_tokens=pt)
+        torch.cuda.synchronize()
+        assert torch.equal(kc2.view(torch.int16), wd.k_cache.view(torch.int16))
+        assert torch.equal(vc2.view(torch.int16), wd.v_cache.view(torch.int16))
+        assert torch.equal(out_h.view(torch.int16), out_d.cpu().view(torch.int16)), name
