@@ -69,7 +69,7 @@ def _check(w, what):
 @pytest.mark.parametrize("hq,hkv,d", [(8, 8, 64), (32, 8, 128), (12, 4, 64), (16, 2, 128), (64, 1, 64)])
 def test_chunked_prefill_matches_the_oracle(hq, hkv, d):
     """Whole prompts and chunks after cached context, for group sizes 1, 3, 4,
-    8 and 64 (a 64-row tile holds 64, 21, 16, 8 and 1 tokens)."""
+    8 and 64 (a 128-row tile holds 128, 42, 32, 16 and 2 tokens)."""
     w = W.make_prefill("chunked_gqa", num_seqs=6, num_q_heads=hq, num_kv_heads=hkv, head_dim=d, new_hi=150,
                        prior_hi=300, seed=hq * 131 + d)
     _check(w, f"chunked hq={hq} hkv={hkv} d={d}")
@@ -132,3 +132,11 @@ def test_full_size_prefill13b_sampled():
         assert np.array_equal(W.to_numpy(getattr(w, name)).view(np.uint8), h[name].view(np.uint8))
     H.assert_close(out[torch.from_numpy(rows).cuda()], ref, "bf16", "prefill13b sample")
     assert bool(torch.all(torch.isfinite(out.float())))
+
+
+def test_short_prompts_stay_within_tolerance():
+    """Prompts of 2..17 tokens (every query sees at most 17 keys), the case the
+    first chunk's weight remainder is there for."""
+    new = tuple(2 + (i % 16) for i in range(96))
+    w = W.make_prefill("chunked_gqa", new_list=new, prior_list=(0,) * len(new), seed=29)
+    _check(w, "short prompts")
