@@ -363,8 +363,8 @@ __device__ __forceinline__ void grid_produce(const CUtensorMap &tmk, const CUten
                     const int y = (b0 + j == last_block) ? last_valid - kBlock : 0;
                     mbar_arrive_expect_tx(&full[st], C::kStage);
                     uint8_t *sk = base + st * C::kStage;
-                    tma_load_4d(sk, &tmk, 0, y, 0, z, &full[st]);
-                    tma_load_4d(sk + C::kTile, &tmv, 0, y, 0, z, &full[st]);
+                    tma_load_4d_hint(sk, &tmk, 0, y, 0, z, &full[st], l2_evict_first());
+                    tma_load_4d_hint(sk + C::kTile, &tmv, 0, y, 0, z, &full[st], l2_evict_first());
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -763,7 +763,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
             const int st = kissued % NS;
             mbar_arrive_expect_tx(&kfull[st], C::kTile);
             uint8_t *sk = ring + st * C::kStage;
-            tma_load_4d(sk, &tmk, 0, y_last, 0, z_last, &kfull[st]);
+            tma_load_4d_hint(sk, &tmk, 0, y_last, 0, z_last, &kfull[st], l2_evict_first());
         }
         ++kissued;
     };
@@ -772,7 +772,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
             const int st = vissued % NS;
             mbar_arrive_expect_tx(&vfull[st], C::kTile);
             uint8_t *sv = ring + st * C::kStage + C::kTile;
-            tma_load_4d(sv, &tmv, 0, y_last, 0, z_last, &vfull[st]);
+            tma_load_4d_hint(sv, &tmv, 0, y_last, 0, z_last, &vfull[st], l2_evict_first());
         }
         ++vissued;
     };
@@ -1032,8 +1032,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
                         stage_info[st] = make_int2(bmem, bearly);
                         mbar_arrive_expect_tx(&full[st], C::kStage);
                         uint8_t *sk = base + st * C::kStage;
-                        tma_load_4d(sk, &tmk, 0, -(bearly & 0xff), 0, zt, &full[st]);
-                        tma_load_4d(sk + C::kTile, &tmv, 0, -(bearly & 0xff), 0, zt, &full[st]);
+                        tma_load_4d_hint(sk, &tmk, 0, -(bearly & 0xff), 0, zt, &full[st], l2_evict_first());
+                        tma_load_4d_hint(sk + C::kTile, &tmv, 0, -(bearly & 0xff), 0, zt, &full[st], l2_evict_first());
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
