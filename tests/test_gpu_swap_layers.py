@@ -134,7 +134,8 @@ def test_multi_layer_null_pointer_is_flagged_not_followed():
     assert b.device_error(clear=True) == b.DEVERR_POINTER
 
 
-# ---- an engine loop: the scheduler drives every device call of each step ----------------
+# ---- an engine loop: the scheduler drives every device call of each step, including the
+# prefill attention of newly admitted prompts ----------------------------------------------
 
 def test_engine_loop_matches_the_oracle_every_step():
     b = H.lib()
@@ -169,7 +170,7 @@ def test_engine_loop_matches_the_oracle_every_step():
     hv = torch.zeros_like(hk).pin_memory()
     sk, sv = _np(dk).copy(), _np(dv).copy()          # host shadows of the device pools
     shk, shv = _np(hk).copy(), _np(hv).copy()
-    steps = swaps_seen = 0
+    steps = swaps_seen = prefills_seen = 0
     while not sched.idle():
         st = sched.step()
         assert st is not None
@@ -190,6 +191,22 @@ def test_engine_loop_matches_the_oracle_every_step():
             kb, vb = bf(kvs[:, 0]), bf(kvs[:, 1])
             b.kv_append(kb.cuda(), vb.cuda(), cuda(np.array(pre_slots, np.int64)), dk, dv)
             oracle.kv_append(_np(kb), _np(vb), np.array(pre_slots, np.int64), sk, sv)
+            # prefill attention of the admitted prompts (causal over their own tokens)
+            n_pre = [n for _, n, _ in st.prefilled]
+            maxb = max(len(tb) for _, _, tb in st.prefilled)
+            ptab = np.zeros((len(n_pre), maxb), np.int32)
+            for i, (_, _, tb) in enumerate(st.prefilled):
+                ptab[i, :len(tb)] = tb
+            plens = np.array(n_pre, np.int32)
+            pqs = np.concatenate([[0], np.cumsum(n_pre)]).astype(np.int32)
+            pq = bf(rng.standard_normal((int(pqs[-1]), Hq, D)).astype(np.float32))
+            pout = torch.empty(pq.shape, dtype=torch.bfloat16, device="cuda")
+            b.paged_prefill_attention(pout, pq.cuda(), dk, dv, cuda(ptab), cuda(plens), cuda(pqs), scale,
+                                      max_query_len=int(plens.max()), max_context_len=int(plens.max()))
+            torch.cuda.synchronize()
+            pref = oracle.paged_prefill_attention(_np(pq), sk, sv, ptab, plens, pqs, scale, Hkv)
+            H.assert_close(pout, pref, "bf16", f"engine step {steps} prefill")
+            prefills_seen += 1
         if len(st.swap_out_pairs):
             b.swap_blocks(hk, hv, dk, dv, cuda(st.swap_out_pairs), host_pairs=st.swap_out_pairs)
             for d, h in st.swap_out_pairs:
@@ -211,4 +228,4 @@ def test_engine_loop_matches_the_oracle_every_step():
         assert np.array_equal(_np(hk).view(np.uint8), shk.view(np.uint8))
         sched.retire(st)
         steps += 1
-    assert sched.preemptions > 0 and sched.swaps > 0 and swaps_seen > 0
+    assert sched.preemptions > 0 and sched.swaps > 0 and swaps_seen > 0 and prefills_seen > 0
