@@ -80,11 +80,17 @@ KERNEL_SOURCES = ["include/pagedkv.h", "paged_kv_cache_177_gb300/csrc/pkv.cu",
 
 
 def kernel_sources_sha256() -> str:
+    """sha256 of the kernel sources with comments and whitespace removed, so
+    that only a change to the code itself invalidates a capture."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 

@@ -1110,7 +1110,7 @@ __global__ void __launch_bounds__(D) cascade_reduce_kernel(const DecodeParams p)
 struct PrefillParams {
     DecodeParams d;
     const int32_t *query_start;  // [S + 1]
-    int tile_tokens;             // query tokens per CTA (16 x consumer warps / g)
+    int tile_tokens;             // query tokens per 128-row tile (128 / g)
     int max_query_len;           // the grid covers this many new tokens per sequence
     int num_queries;             // rows of q and out
 };

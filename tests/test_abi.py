@@ -109,7 +109,7 @@ def test_prefill_rejects_bad_arguments_before_any_cuda_call(lib):
     assert _prefill(lib, dtype=0) == -2              # fp32 prefill is not provided
     assert _prefill(lib, d=96) == -2
     assert _prefill(lib, hq=12, hkv=8) == -1
-    assert _prefill(lib, hq=8 * 65, hkv=8) == -2     # group of 65 > 64 rows per tile
+    assert _prefill(lib, hq=8 * 65, hkv=8) == -2     # group of 65 > the largest supported (64)
     assert _prefill(lib, maxq=-1) == -1
     assert _prefill(lib, qs=None) == -1
     assert _prefill(lib, q=(1 << 12) + 2) == -7
