@@ -1,5 +1,6 @@
 /*
- * pagedkv.h -- C ABI of the GB300 (sm_103a) PagedAttention decode library.
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) PagedAttention library: decode
+ * and prefill attention over a paged KV cache and the block moves around it.
  *
  * The operations follow the pages on PagedAttention and continuous batching:
  *
@@ -19,6 +20,13 @@
  *    still has room is copied when written while other references to it
  *    exist (copy-on-write, "Batching Continuo y PagedAttention", section
  *    "PagedAttention: Memoria virtual para la KV cache").
+ *  - Beyond the decode step: paged_prefill_attention (causal attention of a
+ *    prompt or chunk over the cache), paged_decode_attention_shared_prefix
+ *    (decode reading blocks shared by a group of sequences once), swap_blocks
+ *    (blocks between a device pool and a pinned host pool, for preemption),
+ *    copy_blocks_layers / kv_append_layers (every layer in one launch), and
+ *    paged_decode_attention_static_workspace (decode with library scratch).
+ *    Each cites its passage below.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -35,8 +43,9 @@
  *  - head_dim is 64 or 128; num_q_heads is a multiple of num_kv_heads and the
  *    group size g = num_q_heads / num_kv_heads is at most 16. Query head hq
  *    reads kv head hq / g (consecutive grouping).
- *  - Every pointer is a DEVICE pointer unless stated otherwise, 16-byte
- *    aligned. The caller owns all memory (including the workspace) and the
+ *  - Every pointer is a DEVICE pointer unless stated otherwise (the per-step
+ *    arguments of decode, append and copy may be page-locked host memory),
+ *    16-byte aligned. The caller owns all memory (including the workspace) and the
  *    stream; the library never allocates, frees or synchronises. `stream` is a
  *    cudaStream_t (NULL = the legacy default stream); calls are asynchronous.
  *  - Return value: PKV_OK, or a negative status (pkv_status_string). Only
