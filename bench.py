@@ -12,7 +12,11 @@ Prints one JSON line.  ``value`` is the step's algorithmic bytes (K/V read,
 q read, output written, tables, append and copy traffic) divided by the
 device time of the step, as GB/s, summed over ranks; inputs are resident in
 HBM.  ``e2e`` repeats the measurement with the per-step inputs in pinned host
-memory, copied in, and the output copied back, inside the timed region.
+memory and the output going back there, inside the timed region: through the
+copy engine, and in place (the kernels read and write the pinned host
+buffers over NVLink-C2C); the faster is reported, both are shown.
+``parity`` compares the timed step's output with the oracle on a few
+sequences of the batch.
 Under torchrun every rank runs its own replica of the workload (weak
 scaling): the path has no exchange step.
 """
@@ -255,6 +259,24 @@ def oracle_sample(lay: W.Layout, host: dict, target_s: float, nthreads: int = 0)
         passes += 1
     nbytes = int(lay.context_lens[ids].astype(np.int64).sum()) * per_token
     return nbytes * passes / total / 1e9, total, int(n), passes, nbytes
+
+
+def sampled_parity(lay: W.Layout, host: dict, out: torch.Tensor, dtype: str, n: int = 8):
+    """The timed step's output against the oracle on ``n`` sequences spread over
+    the batch (the host caches already hold the step's copies and appends)."""
+    import oracle
+
+    ids = np.unique(np.linspace(0, lay.spec.num_seqs - 1, n).astype(np.int64))
+    ref = oracle.paged_decode_attention(host["q"], host["k_cache"], host["v_cache"], lay.block_tables,
+                                        lay.context_lens, 1.0 / math.sqrt(lay.spec.head_dim), lay.spec.num_kv_heads,
+                                        seq_ids=ids, nthreads=cpu_cores())
+    got = out[torch.from_numpy(ids).to(out.device)].float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)
+    atol, rtol = (2e-3, 1e-2) if dtype == "bf16" else (1e-5, 1e-5)
+    return {"sample_seqs": int(len(ids)), "max_abs_err": float(err.max()),
+            "max_rel_err": float((err / np.maximum(np.abs(ref), 1e-30)).max()),
+            "bound": f"|gpu - ref| <= {atol:g} + {rtol:g} |ref| per element",
+            "within_bound": bool(np.all(err <= atol + rtol * np.abs(ref)))}
 
 
 def run_reference(args, rank, world, dist):
@@ -500,6 +522,7 @@ def run_ours(args, rank, world, local, dist):
     peak, peak_kind = peaks()
     attn_gbs = nbytes["attention"] / t_attn / 1e9
     cpu = None
+    parity = None
     if world == 1 and not args.no_cpu_baseline:
         # the device caches already hold the step's copies and appends; the oracle
         # re-applies them on the host (idempotent) before attending
@@ -511,6 +534,7 @@ def run_ours(args, rank, world, local, dist):
         g1, s1, n1, p1, b1 = oracle_sample(lay, host, min(3.0, args.cpu_seconds / 3), nthreads=1)
         cpu["single_thread"] = {"value": round(g1, 4), "unit": "GB/s", "cores": 1,
                                 "sample": f"{n1} sequences ({b1 / 1e6:.1f} MB) x {p1} passes in {s1:.1f} s"}
+        parity = sampled_parity(lay, host, out, sp.dtype)
     srt = sorted(step_ms)
     roof_kernel = "decode_bf16_persistent_kernel" if persistent else "decode_bf16_kernel"
     # the captures were taken on the workloads' default launch configuration
@@ -565,6 +589,7 @@ def run_ours(args, rank, world, local, dist):
         "gpu_launches": launches_per_step * steps,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
+        "parity": parity,
         "wall_s_timed_region": round(wall, 3),
     }
     print(json.dumps(line), flush=True)
