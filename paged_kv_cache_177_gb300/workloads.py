@@ -384,6 +384,7 @@ def from_numpy_bits(a: np.ndarray, device="cpu") -> torch.Tensor:
 # =============  =====  =========  ====  =====================================  ==================
 # prefill13b     32     40 / 40    128   lognormal(ln 500, 0.8) in [16, 2048]   0 (whole prompts)
 # chunked_gqa    16     32 / 8     128   uniform int [1, 512]                   uniform [0, 2048]
+# long_prefix    8      32 / 8     128   512 (one chunk)                        uniform [16384, 32768]
 # =============  =====  =========  ====  =====================================  ==================
 
 @dataclass(frozen=True)
@@ -410,6 +411,8 @@ PREFILL_SPECS = {
     "prefill13b": PrefillSpec("prefill13b", 32, 40, 40, 128, "lognormal", 16, 2048, 500.0, 0.8, seed=2001),
     "chunked_gqa": PrefillSpec("chunked_gqa", 16, 32, 8, 128, "uniform", 1, 512, prior_lo=0, prior_hi=2048,
                                seed=2002),
+    "long_prefix": PrefillSpec("long_prefix", 8, 32, 8, 128, "uniform", 512, 512, prior_lo=16384,
+                               prior_hi=32768, seed=2003),
 }
 
 

@@ -140,3 +140,24 @@ def test_short_prompts_stay_within_tolerance():
     new = tuple(2 + (i % 16) for i in range(96))
     w = W.make_prefill("chunked_gqa", new_list=new, prior_list=(0,) * len(new), seed=29)
     _check(w, "short prompts")
+
+
+def test_long_prefix_chunks_sampled():
+    """512-token chunks after 16K-32K cached tokens: four query rows at the
+    start and four at the end of three sequences' chunks, each checked as the
+    last four tokens of a context cut right after them."""
+    w = W.make_prefill("long_prefix", device="cuda")
+    h = _host(w)
+    out = _gpu(w)
+    hs = w.host
+    oracle.kv_append(h["k_new"], h["v_new"], hs["slot_mapping"], h["k_cache"], h["v_cache"])
+    qs, lens = hs["query_start"], hs["context_lens"]
+    for s in (0, 3, 7):
+        n = int(qs[s + 1] - qs[s])
+        for first in (0, n - 4):
+            rows = np.arange(qs[s] + first, qs[s] + first + 4)
+            cut = np.array([lens[s] - n + first + 4], np.int32)
+            ref = oracle.paged_prefill_attention(np.ascontiguousarray(h["q"][rows]), h["k_cache"], h["v_cache"],
+                                                 np.ascontiguousarray(hs["block_tables"][s:s + 1]), cut,
+                                                 np.array([0, 4], np.int32), w.scale, w.spec.num_kv_heads)
+            H.assert_close(out[torch.from_numpy(rows).cuda()], ref, "bf16", f"long prefix seq {s} rows {first}..")
