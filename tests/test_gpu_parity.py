@@ -343,3 +343,17 @@ def test_short_contexts_stay_within_tolerance(partition_tokens):
     out = H.gpu_step(wd, partition_tokens=partition_tokens)
     torch.cuda.synchronize()
     H.assert_close(out, ref, "bf16", f"short contexts, partition_tokens={partition_tokens}")
+
+
+@pytest.mark.parametrize("partition_tokens", [0, -1])
+def test_batch_beyond_the_persistent_kernels_limit(partition_tokens):
+    """9,000 sequences (more than the persistent kernel's 8,192): the call falls
+    back to the grid kernel, balanced request included; lengths 0..47."""
+    lens = tuple(i % 48 for i in range(9000))
+    w = W.make_workload("gqa8b", lengths_list=lens, num_q_heads=8, num_kv_heads=2, head_dim=64, seed=91)
+    h = H.host_arrays(w)
+    ref = H.oracle_step(h, w.layout, w.scale)
+    out = H.gpu_step(w.to("cuda"), partition_tokens=partition_tokens)
+    torch.cuda.synchronize()
+    H.assert_close(out, ref, "bf16", f"9000 sequences, partition_tokens={partition_tokens}")
+    assert torch.all(out[torch.tensor([i for i, n in enumerate(lens) if n == 0], device="cuda")] == 0)
