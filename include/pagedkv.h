@@ -158,6 +158,29 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
                            int partition_tokens, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * One whole decode step in one call ("Batching Continuo y PagedAttention",
+ * cruxr.ai, section "Juntándolo todo: Arquitectura de vLLM": each iteration
+ * copies shared blocks that are about to be written, appends every running
+ * sequence's new token, then runs attention): copy_blocks(src_dst_pairs),
+ * then kv_append(k_new, v_new, slot_mapping), then paged_decode_attention,
+ * with the arguments and semantics of those three calls (num_pairs = 0 or
+ * num_tokens = 0 skips a stage). Every argument is checked before anything
+ * is launched; a failing check launches nothing.
+ * Because the library launches the append itself, the attention kernels are
+ * launched programmatically after it: they read block_tables, context_lens
+ * and q (which the append does not write) while the append still runs, and
+ * wait for it only before reading the caches. Nothing changes for the
+ * caller: work enqueued on the stream before the call finishes before the
+ * step's first launch, as usual.
+ */
+int paged_decode_step(void *out, const void *q, void *k_cache, void *v_cache, const int32_t *block_tables,
+                      const int32_t *context_lens, float scale, int num_kv_heads, int num_seqs, int num_q_heads,
+                      int head_dim, int max_blocks_per_seq, int num_blocks, int max_context_len, pkv_dtype dtype,
+                      int partition_tokens, void *workspace, size_t workspace_bytes, const void *k_new,
+                      const void *v_new, const int64_t *slot_mapping, int num_tokens, const int64_t *src_dst_pairs,
+                      int num_pairs, void *stream);
+
+/*
  * paged_decode_attention for a batch whose sequences share leading blocks --
  * parallel samples of one prompt, a common system prompt ("Batching Continuo
  * y PagedAttention", cruxr.ai, copy-on-write paragraph: the tables of requests

@@ -50,6 +50,8 @@ _shared = _decl("paged_decode_attention_shared_prefix", _i, _vp, _vp, _vp, _vp, 
                 _i, _i, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp)
 _prefill = _decl("paged_prefill_attention", _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i,
                  _i, _i, _i, _vp)
+_step = _decl("paged_decode_step", _i, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp,
+               _sz, _vp, _vp, _vp, _i, _vp, _i, _vp)
 _shared_ws = _decl("pkv_shared_prefix_workspace_bytes", _sz, _i, _i, _i, _i, _i, _i)
 _append = _decl("kv_append", _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
 _copy = _decl("copy_blocks", _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp)
@@ -205,6 +207,39 @@ def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
     decode_raw(decode_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
                            max_context_len=max_context_len, partition_tokens=partition_tokens, workspace=workspace,
                            stream=stream))
+    return out
+
+
+def paged_decode_step(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float, k_new: torch.Tensor,
+                      v_new: torch.Tensor, slot_mapping: torch.Tensor, src_dst_pairs: Optional[torch.Tensor] = None,
+                      *, host_pairs=None, check: bool = True, max_context_len: Optional[int] = None,
+                      partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """One decode step in one call: ``copy_blocks(src_dst_pairs)``, then
+    ``kv_append(k_new, v_new, slot_mapping)``, then ``paged_decode_attention``
+    (arguments as for those calls); the attention's set-up overlaps the
+    append (see include/pagedkv.h)."""
+    args, keep = decode_args(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                             max_context_len=max_context_len, partition_tokens=partition_tokens, workspace=workspace,
+                             stream=stream)
+    _dev_io([k_cache, v_cache], [k_new, v_new, slot_mapping, src_dst_pairs])
+    if not (k_new.dtype == v_new.dtype == k_cache.dtype) or slot_mapping.dtype != torch.int64:
+        raise TypeError("k_new, v_new in the cache dtype and slot_mapping int64")
+    T = k_new.shape[0]
+    NB, Hkv, P, D = k_cache.shape
+    if k_new.shape != (T, Hkv, D) or v_new.shape != k_new.shape or slot_mapping.shape != (T,):
+        raise ValueError("expected k_new, v_new [T, Hkv, D] and slot_mapping [T]")
+    n = 0
+    if src_dst_pairs is not None:
+        if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.numel() % 2:
+            raise TypeError("src_dst_pairs must be int64 [n, 2]")
+        n = src_dst_pairs.numel() // 2
+        if check and n:
+            check_copy_pairs(host_pairs if host_pairs is not None else src_dst_pairs.cpu().numpy(), NB)
+    _check(_step(*args[:-1], _p(k_new), _p(v_new), _p(slot_mapping), T, _p(src_dst_pairs) if n else None, n,
+                 args[-1]), "paged_decode_step")
+    del keep
     return out
 
 

@@ -59,6 +59,24 @@ int check_launch() {
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// Launches `kern` with programmatic stream serialisation: it may start while
+// the previous kernel of the stream runs (that kernel's blocks call
+// pdl_trigger; the new kernel calls pdl_wait before reading what it writes).
+template <typename... Params, typename... Args>
+int launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 // cuTensorMapEncodeTiled from the driver, fetched through the runtime so the
 // library does not link libcuda directly.
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -125,7 +143,7 @@ int max_parts_for(int max_context_len, int part_tokens) {
 
 template <int D, int NT>
 int launch_bf16(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, dim3 grid,
-                cudaStream_t st) {
+                cudaStream_t st, bool pdl = false) {
     using C = pkv::Bf16Cfg<D, NT, kNstage, kNcw>;
     auto kern = pkv::decode_bf16_kernel<D, NT, kNstage, kNcw>;
     static thread_local int configured_device = -1;
@@ -136,13 +154,15 @@ int launch_bf16(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::Decod
             return PKV_ERR_CUDA;
         configured_device = dev;
     }
+    if (pdl) return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmem, st, tmk, tmv, p);
     kern<<<grid, C::kThreads, C::kSmem, st>>>(tmk, tmv, p);
     return check_launch();
 }
 
 template <int D>
-int launch_f32(const pkv::DecodeParams &p, dim3 grid, cudaStream_t st) {
+int launch_f32(const pkv::DecodeParams &p, dim3 grid, cudaStream_t st, bool pdl = false) {
     const size_t smem = (size_t)kNcw * p.group * (D + 2) * sizeof(float);
+    if (pdl) return launch_pdl(pkv::decode_f32_kernel<D, kNcw>, grid, dim3(kNcw * 32), smem, st, p);
     pkv::decode_f32_kernel<D, kNcw><<<grid, kNcw * 32, smem, st>>>(p);
     return check_launch();
 }
@@ -236,7 +256,8 @@ int sm_count(int *n) {
 }
 
 template <int D, int NT, int NS, int NW>
-int launch_persistent(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, cudaStream_t st) {
+int launch_persistent(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, cudaStream_t st,
+                      bool pdl = false) {
     using C = pkv::PersistCfg<D, NT, NS, NW>;
     static_assert(C::smem_bytes(kPersistMaxSeqs) + 64 <= kSmemLimit, "persistent kernel exceeds shared memory");
     auto kern = pkv::decode_bf16_persistent_kernel<D, NT, NS, NW>;
@@ -252,6 +273,7 @@ int launch_persistent(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv:
     int sms = 0;
     if (sm_count(&sms) != PKV_OK) return PKV_ERR_CUDA;
     const int grid = sms < kPersistMaxCtas ? sms : kPersistMaxCtas;
+    if (pdl) return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::smem_bytes(p.num_seqs), st, tmk, tmv, p);
     kern<<<grid, C::kThreads, C::smem_bytes(p.num_seqs), st>>>(tmk, tmv, p);
     return check_launch();
 }
@@ -272,11 +294,16 @@ bool use_persistent(pkv_dtype dtype, int partition_tokens, int num_seqs, int num
     return (long long)num_seqs * num_kv_heads * 4 >= workers;
 }
 
-// Shared by both decode entry points once the workspace is known.
+// How decode_dispatch ends: launch the attention kernels; launch them right
+// after this library's kv_append on the stream (programmatic launch: the
+// set-up overlaps the append, cache reads wait for it); or only check.
+constexpr int kLaunch = 0, kLaunchAfterAppend = 1, kCheckOnly = 2;
+
+// Shared by the decode entry points once the workspace is known.
 int decode_dispatch(void *out, const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
                     const int32_t *context_lens, float scale, int num_kv_heads, int num_seqs, int num_q_heads,
                     int head_dim, int max_blocks_per_seq, int num_blocks, int max_context_len, pkv_dtype dtype,
-                    int partition_tokens, void *workspace, size_t workspace_bytes, void *stream);
+                    int partition_tokens, void *workspace, size_t workspace_bytes, void *stream, int mode = kLaunch);
 }  // namespace
 
 extern "C" {
@@ -335,14 +362,20 @@ int paged_decode_attention(void *out, const void *q, const void *k_cache, const 
                            partition_tokens, workspace, workspace_bytes, stream);
 }
 
-int kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache, void *v_cache, int num_tokens,
-              int num_kv_heads, int head_dim, int num_blocks, pkv_dtype dtype, void *stream) {
+}  // extern "C"
+
+namespace {
+
+int append_impl(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                int num_tokens, int num_kv_heads, int head_dim, int num_blocks, pkv_dtype dtype, void *stream,
+                bool check_only) {
     if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_ARG;
     if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PKV_OK;
     if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_ARG;
     if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
+    if (check_only) return PKV_OK;
     const int vec_per_row = head_dim * elem_bytes(dtype) / 16;
     const long long total = (long long)num_tokens * num_kv_heads * vec_per_row;
     const int threads = 256;
@@ -354,15 +387,29 @@ int kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k
     return check_launch();
 }
 
+}  // namespace
+
+extern "C" {
+
+int kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k_cache, void *v_cache, int num_tokens,
+              int num_kv_heads, int head_dim, int num_blocks, pkv_dtype dtype, void *stream) {
+    return append_impl(k, v, slot_mapping, k_cache, v_cache, num_tokens, num_kv_heads, head_dim, num_blocks, dtype,
+                       stream, false);
+}
+
 int copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs, int num_pairs, int num_kv_heads,
                 int head_dim, int num_blocks, pkv_dtype dtype, void *stream) {
     return swap_blocks(k_cache, v_cache, num_blocks, k_cache, v_cache, num_blocks, src_dst_pairs, num_pairs,
                        num_kv_heads, head_dim, dtype, stream);
 }
 
-int swap_blocks(void *dst_k_cache, void *dst_v_cache, int dst_num_blocks, const void *src_k_cache,
-                const void *src_v_cache, int src_num_blocks, const int64_t *src_dst_pairs, int num_pairs,
-                int num_kv_heads, int head_dim, pkv_dtype dtype, void *stream) {
+}  // extern "C"
+
+namespace {
+
+int move_impl(void *dst_k_cache, void *dst_v_cache, int dst_num_blocks, const void *src_k_cache,
+              const void *src_v_cache, int src_num_blocks, const int64_t *src_dst_pairs, int num_pairs,
+              int num_kv_heads, int head_dim, pkv_dtype dtype, void *stream, bool check_only) {
     if (num_pairs < 0 || num_kv_heads <= 0 || src_num_blocks <= 0 || dst_num_blocks <= 0) return PKV_ERR_ARG;
     if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
@@ -371,6 +418,7 @@ int swap_blocks(void *dst_k_cache, void *dst_v_cache, int dst_num_blocks, const 
     if (!dst_k_cache || !dst_v_cache || !src_k_cache || !src_v_cache || !src_dst_pairs) return PKV_ERR_ARG;
     if (!aligned16(dst_k_cache) || !aligned16(dst_v_cache) || !aligned16(src_k_cache) || !aligned16(src_v_cache))
         return PKV_ERR_ALIGN;
+    if (check_only) return PKV_OK;
     pkv::BlockMove m{};
     m.src[0] = static_cast<const uint4 *>(src_k_cache);
     m.src[1] = static_cast<const uint4 *>(src_v_cache);
@@ -385,6 +433,17 @@ int swap_blocks(void *dst_k_cache, void *dst_v_cache, int dst_num_blocks, const 
     pkv::move_blocks_kernel<<<dim3((unsigned)chunks, num_pairs, 2), threads, 0, static_cast<cudaStream_t>(stream)>>>(
         m, src_dst_pairs);
     return check_launch();
+}
+
+}  // namespace
+
+extern "C" {
+
+int swap_blocks(void *dst_k_cache, void *dst_v_cache, int dst_num_blocks, const void *src_k_cache,
+                const void *src_v_cache, int src_num_blocks, const int64_t *src_dst_pairs, int num_pairs,
+                int num_kv_heads, int head_dim, pkv_dtype dtype, void *stream) {
+    return move_impl(dst_k_cache, dst_v_cache, dst_num_blocks, src_k_cache, src_v_cache, src_num_blocks, src_dst_pairs,
+                     num_pairs, num_kv_heads, head_dim, dtype, stream, false);
 }
 
 int copy_blocks_layers(void *const *k_caches, void *const *v_caches, int num_layers, const int64_t *src_dst_pairs,
@@ -643,7 +702,7 @@ namespace {
 int decode_dispatch(void *out, const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
                     const int32_t *context_lens, float scale, int num_kv_heads, int num_seqs, int num_q_heads,
                     int head_dim, int max_blocks_per_seq, int num_blocks, int max_context_len, pkv_dtype dtype,
-                    int partition_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+                    int partition_tokens, void *workspace, size_t workspace_bytes, void *stream, int mode) {
     if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
         max_context_len < 0 || partition_tokens < PKV_PARTITION_BALANCED)
         return PKV_ERR_ARG;
@@ -666,6 +725,8 @@ int decode_dispatch(void *out, const void *q, const void *k_cache, const void *v
     const size_t need = pkv_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
                                                    partition_tokens);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return PKV_ERR_WORKSPACE;
+    if (mode == kCheckOnly) return PKV_OK;
+    const bool pdl = mode == kLaunchAfterAppend;
 
     pkv::DecodeParams p{};
     p.out = out;
@@ -698,10 +759,10 @@ int decode_dispatch(void *out, const void *q, const void *k_cache, const void *v
         // so their registers fit without spilling
         constexpr int ns128 = PKV_PERSIST_STAGES_D128, ns64 = PKV_PERSIST_STAGES_D64, nw = kPersistWarps;
         if (head_dim == 128)
-            return g <= 8 ? launch_persistent<128, 1, ns128, nw>(tmk, tmv, p, st)
-                          : launch_persistent<128, 2, 2 * ns128, nw / 2>(tmk, tmv, p, st);
-        return g <= 8 ? launch_persistent<64, 1, ns64, nw>(tmk, tmv, p, st)
-                      : launch_persistent<64, 2, 2 * ns64, nw / 2>(tmk, tmv, p, st);
+            return g <= 8 ? launch_persistent<128, 1, ns128, nw>(tmk, tmv, p, st, pdl)
+                          : launch_persistent<128, 2, 2 * ns128, nw / 2>(tmk, tmv, p, st, pdl);
+        return g <= 8 ? launch_persistent<64, 1, ns64, nw>(tmk, tmv, p, st, pdl)
+                      : launch_persistent<64, 2, 2 * ns64, nw / 2>(tmk, tmv, p, st, pdl);
     }
 
     const size_t grid_ws = grid_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, pt);
@@ -714,11 +775,12 @@ int decode_dispatch(void *out, const void *q, const void *k_cache, const void *v
         if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
         if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
         if (head_dim == 128)
-            rc = g <= 8 ? launch_bf16<128, 1>(tmk, tmv, p, grid, st) : launch_bf16<128, 2>(tmk, tmv, p, grid, st);
+            rc = g <= 8 ? launch_bf16<128, 1>(tmk, tmv, p, grid, st, pdl)
+                        : launch_bf16<128, 2>(tmk, tmv, p, grid, st, pdl);
         else
-            rc = g <= 8 ? launch_bf16<64, 1>(tmk, tmv, p, grid, st) : launch_bf16<64, 2>(tmk, tmv, p, grid, st);
+            rc = g <= 8 ? launch_bf16<64, 1>(tmk, tmv, p, grid, st, pdl) : launch_bf16<64, 2>(tmk, tmv, p, grid, st, pdl);
     } else {
-        rc = head_dim == 128 ? launch_f32<128>(p, grid, st) : launch_f32<64>(p, grid, st);
+        rc = head_dim == 128 ? launch_f32<128>(p, grid, st, pdl) : launch_f32<64>(p, grid, st, pdl);
     }
     if (rc != PKV_OK) return rc;
     if (mp > 1) rc = head_dim == 128 ? launch_reduce<128>(p, dtype, st) : launch_reduce<64>(p, dtype, st);
@@ -778,4 +840,42 @@ extern "C" int paged_decode_attention_static_workspace(void *out, const void *q,
     return decode_dispatch(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads, num_seqs,
                            num_q_heads, head_dim, max_blocks_per_seq, num_blocks, max_context_len, dtype,
                            partition_tokens, workspace, workspace ? (size_t)PKV_STATIC_WORKSPACE_BYTES : 0, stream);
+}
+
+// ---------------------------------------------------------------------------
+// One decode step in one call (see pagedkv.h): copy-on-write copies, the KV
+// append, then attention. The library launches the append itself, so it knows
+// the kernel right before the attention writes only the caches: the attention
+// is launched programmatically and reads tables, lengths and queries while the
+// append runs, waiting for it only before its first cache read.
+// ---------------------------------------------------------------------------
+extern "C" int paged_decode_step(void *out, const void *q, void *k_cache, void *v_cache, const int32_t *block_tables,
+                                 const int32_t *context_lens, float scale, int num_kv_heads, int num_seqs,
+                                 int num_q_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
+                                 int max_context_len, pkv_dtype dtype, int partition_tokens, void *workspace,
+                                 size_t workspace_bytes, const void *k_new, const void *v_new,
+                                 const int64_t *slot_mapping, int num_tokens, const int64_t *src_dst_pairs,
+                                 int num_pairs, void *stream) {
+    int rc;
+    // every argument is checked before anything is launched
+    if ((rc = decode_dispatch(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads, num_seqs,
+                              num_q_heads, head_dim, max_blocks_per_seq, num_blocks, max_context_len, dtype,
+                              partition_tokens, workspace, workspace_bytes, stream, kCheckOnly)) != PKV_OK)
+        return rc;
+    if ((rc = append_impl(k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens, num_kv_heads, head_dim, num_blocks,
+                          dtype, stream, true)) != PKV_OK)
+        return rc;
+    if ((rc = move_impl(k_cache, v_cache, num_blocks, k_cache, v_cache, num_blocks, src_dst_pairs, num_pairs,
+                        num_kv_heads, head_dim, dtype, stream, true)) != PKV_OK)
+        return rc;
+    if ((rc = move_impl(k_cache, v_cache, num_blocks, k_cache, v_cache, num_blocks, src_dst_pairs, num_pairs,
+                        num_kv_heads, head_dim, dtype, stream, false)) != PKV_OK)
+        return rc;
+    if ((rc = append_impl(k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens, num_kv_heads, head_dim, num_blocks,
+                          dtype, stream, false)) != PKV_OK)
+        return rc;
+    return decode_dispatch(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads, num_seqs,
+                           num_q_heads, head_dim, max_blocks_per_seq, num_blocks, max_context_len, dtype,
+                           partition_tokens, workspace, workspace_bytes, stream,
+                           num_tokens > 0 ? kLaunchAfterAppend : kLaunch);
 }

@@ -339,6 +339,7 @@ __device__ __forceinline__ void grid_produce(const CUtensorMap &tmk, const CUten
                                              int b0, int nb, int last_block, int last_valid, int num_blocks,
                                              int num_kv_heads, int h, uint8_t *base, uint64_t *full, uint64_t *empty,
                                              int lane) {
+    pdl_wait();  // the caches may have been written by the previous kernel (kv_append in a decode step)
     bool ok = true;
     for (int jb = 0; jb < nb && ok; jb += 32) {
         const int mine = (jb + lane < nb) ? __ldg(table_row + b0 + jb + lane) : 0;
@@ -776,6 +777,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
         }
         ++vissued;
     };
+    pdl_wait();  // the caches may have been written by the previous kernel (kv_append in a decode step)
     while (kissued < min(NS, cnt)) {
         issue_k();
         issue_v();
@@ -1124,6 +1126,7 @@ struct PrefillParams {
 // =====================================================================================
 template <int D, int NCW>
 __global__ void __launch_bounds__(NCW * 32) decode_f32_kernel(const DecodeParams p) {
+    pdl_wait();  // the caches may have been written by the previous kernel (kv_append in a decode step)
     constexpr int PER = D / 32;
     extern __shared__ float fsm[];  // merge buffer: [NCW][g][D + 2]
     const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
@@ -1285,6 +1288,7 @@ __global__ void __launch_bounds__(D *PG) lse_reduce_kernel(const DecodeParams p)
 __global__ void kv_append_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                                  const int64_t *__restrict__ slots, uint4 *__restrict__ kc, uint4 *__restrict__ vc,
                                  int num_tokens, int num_kv_heads, int vec_per_row, int num_blocks) {
+    pdl_trigger();  // a decode step's attention kernel may start its set-up now; it waits for the writes
     const int per_token = num_kv_heads * vec_per_row;
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (long long)num_tokens * per_token) return;

@@ -95,6 +95,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+// A kernel launched with programmatic stream serialisation may start while the
+// previous kernel of its stream is still running, once every block of that
+// kernel has called pdl_trigger() (or exited). pdl_wait() returns when the
+// previous kernel has completed and its memory writes are visible -- at once
+// for a kernel launched the ordinary way -- so a kernel reads nothing the
+// previous one writes before it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- named barrier among a subset of warps ---------------------------------------
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

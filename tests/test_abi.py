@@ -119,6 +119,21 @@ def test_prefill_rejects_bad_arguments_before_any_cuda_call(lib):
     assert _prefill(lib, T=-1) == -1
 
 
+def test_decode_step_checks_everything_before_launching(lib):
+    vp, ci = ctypes.c_void_p, ctypes.c_int
+    f = lib.paged_decode_step
+    f.restype = ci
+    f.argtypes = [vp] * 6 + [ctypes.c_float] + [ci] * 9 + [vp, ctypes.c_size_t, vp, vp, vp, ci, vp, ci, vp]
+    a = 1 << 12
+
+    def call(d=64, T=4, dt=1, pairs=0, kn=a):
+        return f(a, a, a, a, a, a, 0.1, 8, 4, 8, d, 4, 32, 64, dt, 0, a, 1 << 30, kn, a, a, T, a, pairs, None)
+    assert call(d=96) == -2             # attention arguments
+    assert call(T=-1) == -1             # append arguments
+    assert call(kn=a + 8) == -7         # misaligned new keys
+    assert call(dt=7) == -2
+
+
 def test_append_and_copy_reject_bad_arguments(lib):
     vp, ci = ctypes.c_void_p, ctypes.c_int
     ap = lib.kv_append

@@ -357,3 +357,52 @@ def test_batch_beyond_the_persistent_kernels_limit(partition_tokens):
     torch.cuda.synchronize()
     H.assert_close(out, ref, "bf16", f"9000 sequences, partition_tokens={partition_tokens}")
     assert torch.all(out[torch.tensor([i for i, n in enumerate(lens) if n == 0], device="cuda")] == 0)
+
+
+@pytest.mark.parametrize("name,pt,over", [("gqa8b", -1, dict(lengths_list=tuple(range(1, 3000, 97)))),
+                                         ("parallel_sampling", 128, dict(num_prompts=6)),
+                                         ("tiny", 0, {})])
+def test_decode_step_call_matches_the_three_calls(name, pt, over):
+    """paged_decode_step (copies, append, attention launched right after the
+    append) gives the same bits as the three separate calls -- persistent,
+    split-grid and fp32 paths -- directly, replayed from a CUDA graph, and with
+    its per-step arguments in pinned host memory."""
+    b = H.lib()
+    w = W.make_workload(name, seed=55, **over)
+    lay = w.layout
+    ref_d = w.to("cuda")
+    out_ref = H.gpu_step(ref_d, partition_tokens=pt)
+    torch.cuda.synchronize()
+    for variant in ("direct", "graph", "pinned"):
+        d = w.to("cuda")
+        out = torch.full_like(d.q, float("nan"))
+        if variant == "pinned":
+            pin = lambda t: t.contiguous().pin_memory() if t.numel() else t
+            q, kn, vn, sl, bt, cl, pr = (pin(x) for x in (w.q, w.k_new, w.v_new, w.slot_mapping, w.block_tables,
+                                                          w.context_lens, w.cow_pairs))
+            out = torch.full(tuple(w.q.shape), float("nan"), dtype=w.q.dtype).pin_memory()
+        else:
+            q, kn, vn, sl, bt, cl, pr = d.q, d.k_new, d.v_new, d.slot_mapping, d.block_tables, d.context_lens, d.cow_pairs
+        ws = torch.zeros(max(16, b.workspace_bytes(lay.spec.num_seqs, lay.spec.num_q_heads, lay.spec.num_kv_heads,
+                                                   lay.spec.head_dim, lay.max_context_len, pt)),
+                         dtype=torch.uint8, device="cuda")
+
+        def step():
+            b.paged_decode_step(out, q, d.k_cache, d.v_cache, bt, cl, w.scale, kn, vn, sl, pr,
+                                host_pairs=lay.cow_pairs, max_context_len=lay.max_context_len,
+                                partition_tokens=pt, workspace=ws)
+
+        if variant == "graph":
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                step()
+            g.replay()
+        else:
+            step()
+        torch.cuda.synchronize()
+        iv = torch.int16 if w.q.dtype == torch.bfloat16 else torch.int32
+        assert torch.equal(out.cpu().view(iv), out_ref.cpu().view(iv)), f"{name} {variant}"
+        assert torch.equal(d.k_cache.view(iv), ref_d.k_cache.view(iv)) and torch.equal(d.v_cache.view(iv),
+                                                                                        ref_d.v_cache.view(iv))
