@@ -77,6 +77,7 @@ def peaks():
 # workload, valid while the kernel sources still hash to the recorded value.
 PROFILED = {
     ("mha13b", "decode_bf16_persistent_kernel"): "decode_bf16_persistent_kernel_mha13b.md",
+    ("gqa8b", "decode_bf16_persistent_kernel"): "decode_bf16_persistent_kernel_gqa8b.md",
     ("long_context", "decode_bf16_kernel"): "decode_bf16_kernel_long_context.md",
 }
 KERNEL_SOURCES = ["include/pagedkv.h", "paged_kv_cache_177_gb300/csrc/pkv.cu",

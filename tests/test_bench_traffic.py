@@ -26,5 +26,5 @@ def test_traffic_is_null_once_the_sources_change(monkeypatch):
 
 
 def test_traffic_is_null_without_a_capture():
-    t, why = bench.profiled_traffic("gqa8b", "decode_bf16_persistent_kernel")
+    t, why = bench.profiled_traffic("parallel_sampling", "decode_bf16_persistent_kernel")
     assert t is None and "no ncu capture" in why
