@@ -369,7 +369,7 @@ def run_ours(args, rank, world, local, dist):
     stream = torch.cuda.Stream(dev)
     has_pairs = len(lay.cow_pairs) > 0
     attn_launches = B.decode_launches(S, Hkv, maxlen, pt, w.q.dtype)
-    persistent = pt <= 0 and sp.dtype == "bf16" and attn_launches == 1 and maxlen > B.partition_tokens(S, Hkv, maxlen, pt)
+    persistent = B.decode_persistent(S, Hkv, pt, w.q.dtype)
     launches_per_step = (1 if has_pairs else 0) + 1 + attn_launches
     B.check_copy_pairs(lay.cow_pairs, lay.num_blocks)
     # per-step inputs live in buffers of their own, so the end-to-end run can

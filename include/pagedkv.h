@@ -120,6 +120,15 @@ int pkv_decode_partition_tokens(int num_seqs, int num_kv_heads, int max_context_
 int pkv_decode_launches(int num_seqs, int num_kv_heads, int max_context_len, int partition_tokens, pkv_dtype dtype);
 
 /*
+ * 1 if paged_decode_attention with these arguments runs the persistent
+ * balanced kernel (bf16 only: PKV_PARTITION_BALANCED, or automatic
+ * partitioning on a batch with at least a quarter as many (sequence, kv head)
+ * units as the GPU has persistent warps), else 0. Queries the current
+ * device's SM count.
+ */
+int pkv_decode_persistent(int num_seqs, int num_kv_heads, int partition_tokens, pkv_dtype dtype);
+
+/*
  * Bytes of device workspace paged_decode_attention needs with these
  * arguments (0 when it needs none). The workspace holds per-sequence arrival
  * counters and partial softmax states (max in the log2 domain, sum, partial

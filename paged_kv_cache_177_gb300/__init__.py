@@ -14,8 +14,10 @@ __version__ = "0.1.0"
 
 _BINDING_NAMES = {
     "paged_decode_attention", "kv_append", "copy_blocks", "check_copy_pairs", "validate", "validate_slots",
-    "swap_blocks", "check_swap_pairs", "paged_decode_attention_shared_prefix", "paged_prefill_attention", "paged_decode_step", "shared_prefix_workspace_bytes", "prefix_groups", "copy_blocks_layers", "kv_append_layers", "layer_pointers",
-    "device_error", "workspace_bytes", "partition_tokens", "decode_launches", "status_string", "version", "PagedKVError",
+    "swap_blocks", "check_swap_pairs", "paged_decode_attention_shared_prefix", "paged_prefill_attention",
+    "paged_decode_step", "shared_prefix_workspace_bytes", "prefix_groups", "copy_blocks_layers", "kv_append_layers",
+    "layer_pointers", "device_error", "workspace_bytes", "partition_tokens", "decode_launches", "decode_persistent",
+    "status_string", "version", "PagedKVError",
 }
 
 

@@ -44,6 +44,7 @@ _version = _decl("pkv_version", _i)
 _partition_tokens = _decl("pkv_decode_partition_tokens", _i, _i, _i, _i, _i)
 _workspace_bytes = _decl("pkv_decode_workspace_bytes", _sz, _i, _i, _i, _i, _i, _i)
 _decode_launches = _decl("pkv_decode_launches", _i, _i, _i, _i, _i, _i)
+_decode_persistent = _decl("pkv_decode_persistent", _i, _i, _i, _i, _i)
 _decode = _decl("paged_decode_attention", _i, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                 _vp, _sz, _vp)
 _shared = _decl("paged_decode_attention_shared_prefix", _i, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i,
@@ -146,6 +147,14 @@ def decode_launches(num_seqs: int, num_kv_heads: int, max_context_len: int, part
     return int(_decode_launches(num_seqs, num_kv_heads, max_context_len, partition_tokens, code))
 
 
+def decode_persistent(num_seqs: int, num_kv_heads: int, partition_tokens: int = 0,
+                      dtype: torch.dtype = torch.bfloat16) -> bool:
+    """Whether a decode call with these arguments runs the persistent
+    balanced kernel."""
+    code = PKV_BF16 if dtype == torch.bfloat16 else PKV_F32
+    return bool(_decode_persistent(num_seqs, num_kv_heads, partition_tokens, code))
+
+
 def decode_args(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                 block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                 num_kv_heads: Optional[int] = None, *, max_context_len: Optional[int] = None,
@@ -200,7 +209,8 @@ def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
     ``partition_tokens``: 0 automatic, -1 balanced (persistent kernel, bf16),
     > 0 fixed partitions of that many tokens.
     A caller-provided ``workspace`` must have been zero-filled once before
-    its first use; the library leaves it zero-filled after each call.
+    its first use; the library leaves the part that must start at zero at
+    zero after each call, so it is reused without clearing.
     q, out, block_tables and context_lens may be pinned host tensors: the
     kernels then read and write them in place (no separate copy).
     """

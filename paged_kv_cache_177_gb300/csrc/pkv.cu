@@ -343,6 +343,11 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
     return pers > grid_ws ? pers : grid_ws;
 }
 
+int pkv_decode_persistent(int num_seqs, int num_kv_heads, int partition_tokens, pkv_dtype dtype) {
+    if (num_seqs <= 0 || num_kv_heads <= 0 || partition_tokens < PKV_PARTITION_BALANCED) return 0;
+    return use_persistent(dtype, partition_tokens, num_seqs, num_kv_heads) ? 1 : 0;
+}
+
 int pkv_decode_launches(int num_seqs, int num_kv_heads, int max_context_len, int partition_tokens, pkv_dtype dtype) {
     if (num_seqs <= 0 || num_kv_heads <= 0) return 0;
     if (partition_tokens < PKV_PARTITION_BALANCED) return 0;

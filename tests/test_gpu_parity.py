@@ -254,6 +254,7 @@ def test_persistent_path_leaves_counters_zero_and_repeats_bit_identically():
         w = wc.to("cuda")
         H.gpu_step(w, attention=False)
         lay = w.layout
+        assert b.decode_persistent(lay.spec.num_seqs, hkv, -1, torch.bfloat16)
         assert b.decode_launches(lay.spec.num_seqs, hkv, lay.max_context_len, -1, torch.bfloat16) == 1
         need = b.workspace_bytes(lay.spec.num_seqs, hq, hkv, 128, lay.max_context_len, -1)
         ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
@@ -269,6 +270,51 @@ def test_persistent_path_leaves_counters_zero_and_repeats_bit_identically():
         assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
         ref = H.oracle_step(h, lay, w.scale)
         H.assert_close(outs[0], ref, "bf16", f"persistent {lens}")
+
+
+LARGE_CASES = [
+    # name, Hq, Hkv, sequences, longest context
+    ("mha_large", 16, 16, 128, 1200),
+    ("gqa8_large", 64, 8, 256, 1200),
+    ("gqa4_large", 16, 4, 256, 1200),
+]
+
+
+@pytest.mark.parametrize("case", LARGE_CASES, ids=[c[0] for c in LARGE_CASES])
+def test_persistent_large_batches(case):
+    """Batches of at least 8 positions per persistent warp: every warp's
+    range cuts units at both ends, so nearly every warp writes segment
+    states and many merge; the arrival counters are zero after each call, the
+    output repeats bit for bit and matches the oracle on sampled sequences."""
+    name, hq, hkv, S, longest = case
+    b = H.lib()
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
+    lens = tuple(int(x) for x in rng.integers(1, longest + 1, S))
+    wc = W.make_workload("gqa8b", lengths_list=lens, num_q_heads=hq, num_kv_heads=hkv, seed=S + hq)
+    h = H.host_arrays(wc)
+    w = wc.to("cuda")
+    H.gpu_step(w, attention=False)
+    lay = w.layout
+    assert hkv * sum((x + 15) // 16 for x in lens) >= 8 * 152 * 16
+    assert b.decode_persistent(S, hkv, -1, torch.bfloat16)
+    ws = torch.zeros(b.workspace_bytes(S, hq, hkv, 128, lay.max_context_len, -1), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        out = torch.empty_like(w.q)
+        b.paged_decode_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
+                                 max_context_len=lay.max_context_len, workspace=ws, partition_tokens=-1)
+        torch.cuda.synchronize()
+        assert int(ws[: S * hkv * 4].count_nonzero()) == 0
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    order = np.argsort(np.asarray(lens), kind="stable")
+    pick = sorted(set([int(order[0]), int(order[-1])] + rng.choice(S, 10, replace=False).tolist()))
+    ref = H.oracle_step(h, lay, w.scale, seq_ids=pick)
+    H.assert_close(outs[0][torch.as_tensor(pick, device="cuda")], ref, "bf16", name)
+    o = outs[0].float()
+    assert torch.isfinite(o).all()
+    vmax = torch.nan_to_num(w.v_cache.float(), nan=0.0).abs().max()   # free blocks hold NaN
+    assert float(o.abs().max()) <= float(vmax) * (1 + 1e-2)
 
 
 def test_persistent_step_in_a_cuda_graph():
