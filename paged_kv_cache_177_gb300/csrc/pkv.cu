@@ -611,6 +611,7 @@ int paged_prefill_attention(void *out, const void *q, const void *k_cache, const
     const int tile_tokens = 128 / g;  // 128 query rows per tile, two tiles per CTA
     const int tiles = (max_query_len + tile_tokens - 1) / tile_tokens;
     const int pairs = (tiles + 1) / 2;
+    if (pairs > 65535) return PKV_ERR_UNSUPPORTED;
     if (num_seqs == 0 || max_query_len == 0 || num_queries == 0) return PKV_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start) return PKV_ERR_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
@@ -637,7 +638,9 @@ int paged_prefill_attention(void *out, const void *q, const void *k_cache, const
     pp.num_queries = num_queries;
     alignas(64) CUtensorMap tmk, tmv;
     int rc;
-    const dim3 grid(pairs, num_kv_heads, num_seqs);
+    // pair index slowest: CTAs start in linear order, so every sequence's
+    // last (longest) pair starts before any shorter one
+    const dim3 grid(num_kv_heads, num_seqs, pairs);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     alignas(64) CUtensorMap tmq;
     if ((rc = encode_q_map(&tmq, q, num_queries, num_q_heads, head_dim, g, tile_tokens)) != PKV_OK) return rc;

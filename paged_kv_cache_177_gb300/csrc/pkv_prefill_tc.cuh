@@ -106,15 +106,15 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
     using C = TcCfg<D>;
     const DecodeParams &p = pp.d;
     extern __shared__ uint8_t smem_raw[];
-    const int h = blockIdx.y, s = blockIdx.z;
-    const int pair = gridDim.x - 1 - blockIdx.x;  // the longest (last) tiles start first
+    const int h = blockIdx.x, s = blockIdx.y;
+    const int pair = gridDim.z - 1 - blockIdx.z;  // the longest (last) tiles start first
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = p.group;
     const int q0 = __ldg(pp.query_start + s), n = __ldg(pp.query_start + s + 1) - q0;
-    const int len = seq_len(p, s, tid == 0 && blockIdx.x == 0 && h == 0);
+    const int len = seq_len(p, s, tid == 0 && blockIdx.z == 0 && h == 0);
     const int tt = pp.tile_tokens;
     if (n < 0 || n > len || n > pp.max_query_len || q0 < 0 || q0 + n > pp.num_queries) {
-        if (tid == 0 && blockIdx.x == 0 && h == 0) raise_error(PKV_DEVERR_LENGTH);
+        if (tid == 0 && blockIdx.z == 0 && h == 0) raise_error(PKV_DEVERR_LENGTH);
         return;
     }
     if (pair * C::kTiles * tt >= n) return;

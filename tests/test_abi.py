@@ -117,6 +117,9 @@ def test_prefill_rejects_bad_arguments_before_any_cuda_call(lib):
     assert _prefill(lib, S=0) == 0
     assert _prefill(lib, maxq=0) == 0                # no new tokens: nothing to do
     assert _prefill(lib, T=-1) == -1
+    # more than 65,535 pairs of query tiles (the grid's pair dimension): 64 heads in one group
+    # make 2-token tiles, so 2**18 new tokens are 65,536 pairs
+    assert _prefill(lib, hq=64, hkv=1, maxq=1 << 18, T=1 << 18) == -2
 
 
 def test_decode_step_checks_everything_before_launching(lib):
