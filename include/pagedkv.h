@@ -20,6 +20,8 @@
  *    still has room is copied when written while other references to it
  *    exist (copy-on-write, "Batching Continuo y PagedAttention", section
  *    "PagedAttention: Memoria virtual para la KV cache").
+ *  - paged_decode_step: the three calls above as one decode step (copies,
+ *    append, attention), every argument checked before anything launches.
  *  - Beyond the decode step: paged_prefill_attention (causal attention of a
  *    prompt or chunk over the cache), paged_decode_attention_shared_prefix
  *    (decode reading blocks shared by a group of sequences once), swap_blocks
