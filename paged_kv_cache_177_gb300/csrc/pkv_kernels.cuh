@@ -865,17 +865,16 @@ __global__ void __launch_bounds__(NW * 32, 1)
                         for (int mt = 0; mt < C::kSteps; ++mt) row[2 + 16 * mt + gq + (e >> 1) * 8] = wa.acc[mt][nt][e];
                     }
                 }
-            __threadfence();
-            __syncwarp();
+            __syncwarp();  // every lane's state writes are ordered before lane 0's release below
             const int u = c.s * Hkv + c.h;
             int prev = 0;
-            if (lane == 0) prev = atomicAdd(p.counters + u, 1);
+            if (lane == 0) prev = atomic_add_acq_rel_gpu(p.counters + u, 1);
             prev = __shfl_sync(0xffffffffu, prev, 0);
             const long long x0 = (long long)Hkv * prefix[c.s] + (long long)c.h * c.n;
             const int w1 = (int)(((x0 + 1) * W - 1) / T);
             const int w2 = (int)(((x0 + c.n) * W - 1) / T);
             if (prev == w2 - w1) {
-                __threadfence();
+                __syncwarp();  // lane 0's acquire covers the lanes reading the other segments
                 merge_segments<D>(p.partials, slot_floats, w1, w2 - w1 + 1, g, out + orow0 * D, lane);
                 if (lane == 0) p.counters[u] = 0;  // ready for the next call
             }

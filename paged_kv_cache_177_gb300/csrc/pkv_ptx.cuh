@@ -175,6 +175,16 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// atomicAdd with acquire-release ordering at GPU scope: the writes this thread
+// made (and those of threads it synchronised with before) are visible to
+// whoever observes the increment, and when the returned count shows this is
+// the last arrival, the writes of the earlier arrivals are visible here.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the
 // async proxy (tensor-core operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
