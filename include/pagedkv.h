@@ -206,7 +206,7 @@ int paged_decode_step(void *out, const void *q, void *k_cache, void *v_cache, co
  * group_members: int32 [num_groups][group_size], sequence ids (-1 = empty
  *   slot). The groups partition the batch: every sequence is listed exactly
  *   once, a sequence that shares nothing as a group of one (a sequence not
- *   listed gets no output).
+ *   listed gets no output); so num_groups <= num_seqs (else PKV_ERR_ARG).
  * shared_blocks: int32 [num_groups]: leading blocks all members' tables hold
  *   in common (same physical ids). The kernel uses at most the full blocks of
  *   the group's shortest member and reads them through the first member's

@@ -182,7 +182,9 @@ int launch_cascade(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::De
     }
     kern<<<grid, C::kThreads, C::kSmem, st>>>(tmk, tmv, p);
     if (check_launch() != PKV_OK) return PKV_ERR_CUDA;
-    pkv::cascade_reduce_kernel<D><<<dim3(p.num_q_heads, p.group_size, p.num_groups), D, 0, st>>>(p);
+    const long long rows = (long long)p.num_groups * p.group_size * p.num_q_heads;  // one warp each
+    pkv::cascade_reduce_kernel<D>
+        <<<(unsigned)((rows + pkv::kReduceWarps - 1) / pkv::kReduceWarps), pkv::kReduceWarps * 32, 0, st>>>(p);
     return check_launch();
 }
 
@@ -522,7 +524,9 @@ size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int head
     const int pt = pkv_decode_partition_tokens(num_seqs, 1, max_context_len, partition_tokens);
     if (pt % 16 != 0) return 0;
     const int parts = cascade_parts(group_size, max_context_len, pt);
-    return (size_t)num_seqs * num_q_heads * (size_t)(parts > 0 ? parts : 1) * (2 + (size_t)head_dim) * sizeof(float);
+    // partition states, then each group's partition count (groups <= sequences)
+    return (size_t)num_seqs * num_q_heads * (size_t)(parts > 0 ? parts : 1) * (2 + (size_t)head_dim) * sizeof(float) +
+           (size_t)num_seqs * sizeof(int);
 }
 
 int paged_decode_attention_shared_prefix(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -546,6 +550,7 @@ int paged_decode_attention_shared_prefix(void *out, const void *q, const void *k
     if (num_seqs == 0) return PKV_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_ARG;
     if (num_groups > 0 && (!group_members || !shared_blocks)) return PKV_ERR_ARG;
+    if (num_groups > num_seqs) return PKV_ERR_ARG;  // every sequence is in exactly one group
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGN;
     const int pt = pkv_decode_partition_tokens(num_seqs, num_kv_heads, max_context_len, partition_tokens);
     if (pt % 16 != 0) return PKV_ERR_ARG;
@@ -575,6 +580,7 @@ int paged_decode_attention_shared_prefix(void *out, const void *q, const void *k
     p.pre_parts = 0;
     p.ws_ml = static_cast<float *>(workspace);
     p.ws_o = static_cast<float *>(workspace) + (size_t)num_seqs * num_q_heads * p.max_parts * 2;
+    p.counters = reinterpret_cast<int *>(p.ws_o + (size_t)num_seqs * num_q_heads * p.max_parts * head_dim);
     p.group_members = group_members;
     p.shared_blocks = shared_blocks;
     p.num_groups = num_groups;

@@ -55,7 +55,8 @@ struct DecodeParams {
     int max_blocks_per_seq, num_blocks, max_context_len;
     int part_blocks;              // blocks per split-context partition
     int max_parts;                // partitions allotted per (sequence, head) in the workspace
-    int *counters;                // persistent kernel: [S][Hkv] arrival counters, zero between calls
+    int *counters;                // persistent kernel: [S][Hkv] arrival counters, zero between calls;
+                                  // shared-prefix kernel: [groups] partitions of each group's union
     float *partials;              // persistent kernel: [workers][2][g][2 + D] segment states
     // shared-prefix (cascade) decode
     const int32_t *group_members; // [num_groups][group_size] sequence ids, -1 = empty
@@ -973,6 +974,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
     const int g = p.group;
     if (warp == 0) union_unit(p, z, u, lane, part == 0 && h == 0);
     __syncthreads();
+    if (part == 0 && h == 0 && tid == 0)  // for the reduce: how many partitions the group's rows have
+        p.counters[z] = u.count ? (u.total + p.part_blocks - 1) / p.part_blocks : 0;
     const int j0 = part * p.part_blocks;
     if (u.count == 0 || j0 >= u.total) return;
     const int nb = min(u.total - j0, p.part_blocks);
@@ -1072,38 +1075,79 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
 }
 
 // Merges each (sequence, query head) row's partition states (log-sum-exp
-// rule, empty states skipped); a row with none gives zeros. One CTA of D
-// threads per (query head, member slot, group).
+// rule, empty states skipped); a row with none gives zeros. One warp per
+// (group, member slot, query head): lane k holds partition k's (max, sum),
+// every lane accumulates head-dim elements lane, lane + 32, .., with the
+// partition outputs of up to kReduceBatch partitions in flight at a time.
+constexpr int kReduceWarps = 8, kReduceBatch = 8;
 template <int D>
-__global__ void __launch_bounds__(D) cascade_reduce_kernel(const DecodeParams p) {
-    __shared__ float scratch[32];
-    __shared__ UnionUnit u;
-    const int hq = blockIdx.x, m = blockIdx.y, z = blockIdx.z, tid = threadIdx.x;
-    const int s = __ldg(p.group_members + (size_t)z * p.group_size + m);
+__global__ void __launch_bounds__(kReduceWarps * 32) cascade_reduce_kernel(const DecodeParams p) {
+    constexpr int PER = D / 32;
+    const int lane = threadIdx.x & 31, Hq = p.num_q_heads, M = p.group_size;
+    const long long r = (long long)blockIdx.x * kReduceWarps + (threadIdx.x >> 5);
+    if (r >= (long long)p.num_groups * M * Hq) return;
+    const int hq = (int)(r % Hq);
+    const long long zm = r / Hq;
+    const int m = (int)(zm % M), z = (int)(zm / M);
+    const int s = __ldg(p.group_members + (size_t)z * M + m);
+    const int n = __ldcg(p.counters + z);  // the group's partitions (written by the shared-prefix kernel)
     if (s < 0 || s >= p.num_seqs) return;
-    if (tid < 32) union_unit(p, z, u, tid, false);
-    __syncthreads();
-    const int n = (u.total + p.part_blocks - 1) / p.part_blocks;
-    const size_t row = (size_t)s * p.num_q_heads + hq;
+    const size_t row = (size_t)s * Hq + hq;
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out) + row * D;
     const float *ml = p.ws_ml + row * p.max_parts * 2;
     const float *o = p.ws_o + row * p.max_parts * D;
-    float Mx = -INFINITY;
-    for (int k = tid; k < n; k += D) Mx = fmaxf(Mx, ml[2 * k]);
-    Mx = block_reduce(Mx, true, scratch);
+    // the row's max and weight sum over all partitions, 32 per pass
+    float Mx = -INFINITY, W = 0.f;
+    for (int k0 = 0; k0 < n; k0 += 32) {
+        float mk = -INFINITY, lk = 0.f;
+        if (k0 + lane < n) {
+            const float2 v = __ldcg(reinterpret_cast<const float2 *>(ml) + k0 + lane);
+            mk = v.x;
+            lk = v.y;
+        }
+        float Mp = mk;
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, sh));
+        float Wp = mk == -INFINITY ? 0.f : lk * exp2f(mk - Mp);
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) Wp += __shfl_xor_sync(0xffffffffu, Wp, sh);
+        const float Mn = fmaxf(Mx, Mp);
+        W = (Mx == -INFINITY ? 0.f : W * exp2f(Mx - Mn)) + (Mp == -INFINITY ? 0.f : Wp * exp2f(Mp - Mn));
+        Mx = Mn;
+    }
     if (Mx == -INFINITY) {  // nothing attended: empty context
-        out[tid] = __float2bfloat16_rn(0.f);
+#pragma unroll
+        for (int i = 0; i < PER; ++i) out[lane + 32 * i] = __float2bfloat16_rn(0.f);
         return;
     }
-    float W = 0.f, acc = 0.f;
-    for (int k = 0; k < n; ++k) {
-        const float mk = ml[2 * k];
-        if (mk == -INFINITY) continue;
-        const float w = ml[2 * k + 1] * exp2f(mk - Mx);
-        W += w;
-        acc = fmaf(w, o[(size_t)k * D + tid], acc);
+    const float invW = 1.f / W;
+    float acc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+    float ck = 0.f;  // lane k: the weight of partition (32-block base) + k
+    for (int k0 = 0; k0 < n; k0 += kReduceBatch) {
+        if ((k0 & 31) == 0) {
+            const int k = k0 + lane;
+            ck = 0.f;
+            if (k < n) {
+                const float2 v = __ldcg(reinterpret_cast<const float2 *>(ml) + k);
+                ck = v.x == -INFINITY ? 0.f : v.y * exp2f(v.x - Mx) * invW;
+            }
+        }
+        float vals[kReduceBatch][PER];
+#pragma unroll
+        for (int b = 0; b < kReduceBatch; ++b)
+#pragma unroll
+            for (int i = 0; i < PER; ++i) vals[b][i] = k0 + b < n ? __ldcg(o + (size_t)(k0 + b) * D + lane + 32 * i) : 0.f;
+#pragma unroll
+        for (int b = 0; b < kReduceBatch; ++b) {
+            const float c = __shfl_sync(0xffffffffu, ck, (k0 + b) & 31);
+#pragma unroll
+            for (int i = 0; i < PER; ++i) acc[i] = fmaf(c, vals[b][i], acc[i]);
+        }
     }
-    out[tid] = __float2bfloat16_rn(acc / W);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) out[lane + 32 * i] = __float2bfloat16_rn(acc[i]);
 }
 
 // Prefill (bf16) parameters: causal attention for several new tokens per
