@@ -7,6 +7,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 from paged_kv_cache_177_gb300.build import INCLUDE, build_library
 
@@ -61,6 +62,23 @@ def test_partition_and_workspace_sizing(binding):
     # otherwise: S * Hq * ceil(L / P) * (2 + D) floats
     assert binding.workspace_bytes(8, 64, 8, 128, 131072, 512) == 8 * 64 * 256 * 130 * 4
     assert binding.workspace_bytes(2, 4, 4, 64, 1000, 64) == 2 * 4 * 16 * 66 * 4
+
+
+def test_which_decode_kernel_runs(binding):
+    """The planning queries agree on the path: the balanced split always
+    runs the persistent kernel (one launch), fixed partitions and fp32 never
+    do; bad arguments give 0. (Without a GPU the SM count defaults to the
+    largest the workspace is sized for.)"""
+    bf16, f32 = torch.bfloat16, torch.float32
+    assert binding.decode_persistent(64, 40, -1, bf16)
+    assert binding.decode_launches(64, 40, 4096, -1, bf16) == 1
+    assert not binding.decode_persistent(64, 40, 512, bf16)
+    assert binding.decode_launches(64, 40, 4096, 512, bf16) == 2
+    assert not binding.decode_persistent(64, 40, -1, f32)
+    assert not binding.decode_persistent(0, 40, -1, bf16) and not binding.decode_persistent(64, 40, -2, bf16)
+    # automatic: a quarter as many units as persistent warps or more
+    assert binding.decode_persistent(8192, 8, 0, bf16)
+    assert not binding.decode_persistent(8, 8, 0, bf16)
 
 
 def _decode(lib, **kw):
