@@ -3,7 +3,8 @@
 A step is one pass of the whole hot path over one batch of the workload:
 copy-on-write block copies (when the workload has any), the KV append of
 this step's tokens, and paged decode attention (split-context partitions and
-their log-sum-exp reduce included) for every sequence.
+their log-sum-exp reduce included) for every sequence -- one
+paged_decode_step call, captured once as a CUDA graph and replayed.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mha13b]
     python bench.py --impl reference ...     # the fp64 CPU oracle on the host cores
