@@ -88,3 +88,33 @@ def test_full_size_parallel_sampling_against_plain_decode():
     H.assert_close(out[torch.tensor(pick, device="cuda")], ref, "bf16", "full size shared prefix")
     diff = (out.float() - plain.float()).abs()
     assert float(diff.max()) < 4e-3 + 2e-2 * float(plain.float().abs().max())
+
+
+def test_one_uncleared_workspace_serves_every_partition_size():
+    """One workspace, filled with garbage once and never cleared, serves calls
+    with different partition sizes (a union of one partition, and unions cut
+    into many): each call matches the oracle and repeats bit for bit."""
+    wc = W.make_workload("parallel_sampling", num_prompts=5)
+    h = H.host_arrays(wc)
+    ref = H.oracle_step(h, wc.layout, wc.scale)
+    w = wc.to("cuda")
+    H.gpu_step(w, attention=False)
+    lay = w.layout
+    b = H.lib()
+    sp = lay.spec
+    groups = torch.from_numpy(lay.group_members).cuda()
+    shared = torch.from_numpy(lay.shared_blocks).cuda()
+    need = max(b.shared_prefix_workspace_bytes(sp.num_seqs, sp.num_q_heads, sp.head_dim, lay.max_context_len,
+                                               groups.shape[1], pt) for pt in (64, 512, 4096))
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    for pt in (64, 4096, 512, 64):
+        outs = []
+        for _ in range(3):
+            out = torch.full_like(w.q, float("nan"))
+            b.paged_decode_attention_shared_prefix(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                                                   w.scale, groups, shared, max_context_len=lay.max_context_len,
+                                                   partition_tokens=pt, workspace=ws)
+            torch.cuda.synchronize()
+            outs.append(out)
+        H.assert_close(outs[0], ref, "bf16", f"shared prefix, partition_tokens={pt}")
+        assert all(torch.equal(outs[0], o) for o in outs[1:]), f"partition_tokens={pt}: repeat differs"
