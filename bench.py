@@ -652,14 +652,24 @@ def run_op(args, rank, world, local, dist):
                            dtype=torch.uint8, device=dev)
         ws_p = torch.zeros(max(16, B.workspace_bytes(sp.num_seqs, H, sp.num_kv_heads, sp.head_dim, maxlen)),
                            dtype=torch.uint8, device=dev)
-        B.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
+        # the step's writes, in the step's order: copy-on-write copies, then the new tokens
         B.copy_blocks(w.k_cache, w.v_cache, w.cow_pairs, host_pairs=lay.cow_pairs)
+        B.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
         t_c = time_it(lambda: B.paged_decode_attention_shared_prefix(
             out_c, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, groups, shared,
             max_context_len=maxlen, workspace=ws_c), args.steps or 50)
         t_p = time_it(lambda: B.paged_decode_attention(
             out_p, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, max_context_len=maxlen,
             workspace=ws_p), args.steps or 50)
+        # both calls attend the same contexts: finite outputs that agree to the bf16 tolerance
+        torch.cuda.synchronize(dev)
+        if not (bool(torch.isfinite(out_c.float()).all()) and bool(torch.isfinite(out_p.float()).all())):
+            raise RuntimeError("non-finite attention output in the shared-prefix benchmark")
+        diff = float((out_c.float() - out_p.float()).abs().max())
+        if diff > 4e-3 + 2e-2 * float(out_p.float().abs().max()):
+            raise RuntimeError(f"shared-prefix and plain decode outputs differ by {diff}")
+        if B.device_error(clear=True):
+            raise RuntimeError("device error word set during the shared-prefix benchmark")
         logical, unique = lay.kv_bytes(eb), lay.unique_kv_bytes(eb)
         peak, kind = peaks()
         line = {"metric": "shared-prefix decode attention, logical KV GB/s", "unit": "GB/s",
@@ -669,6 +679,7 @@ def run_op(args, rank, world, local, dist):
                                   "unique_frac_of_peak": round(unique / t_c / 1e9 / peak, 4)},
                 "plain_decode": {"us": round(t_p * 1e6, 2), "logical_GB/s": round(logical / t_p / 1e9, 2)},
                 "speedup": round(t_p / t_c, 3), "logical_bytes": int(logical), "unique_bytes": int(unique),
+                "max_abs_diff_vs_plain_decode": diff,
                 "peak": peak, "peak_kind": kind, "higher_is_better": True,
                 "config": {"workload": describe(sp), "groups": int(groups.shape[0]),
                            "shared_blocks": int(lay.shared_blocks[0])}}
