@@ -783,6 +783,23 @@ def run_prefill(args, dev, B):
     n = args.steps or 30
     t_step = graph_time(step, n, dev, evict)
     t_attn = graph_time(attention, n, dev, evict)
+    # Each prompt's last query row attends its whole context: the decode kernels (mma.sync,
+    # no code shared with the tcgen05 prefill kernel) must give the same row.
+    torch.cuda.synchronize(dev)
+    if not bool(torch.isfinite(out.float()).all()):
+        raise RuntimeError("non-finite prefill attention output")
+    qs = w.query_start.to(torch.int64)
+    has = (qs[1:] > qs[:-1]).nonzero().flatten()
+    last = qs[1:][has] - 1
+    dec = torch.empty((len(has),) + tuple(w.q.shape[1:]), dtype=w.q.dtype, device=dev)
+    B.paged_decode_attention(dec, w.q[last].contiguous(), w.k_cache, w.v_cache, w.block_tables[has].contiguous(),
+                             w.context_lens[has].contiguous(), w.scale, max_context_len=mc)
+    torch.cuda.synchronize(dev)
+    diff = float((out[last].float() - dec.float()).abs().max())
+    if diff > 4e-3 + 2e-2 * float(dec.float().abs().max()):
+        raise RuntimeError(f"prefill's last rows differ from decode by {diff}")
+    if B.device_error(clear=True):
+        raise RuntimeError("device error word set during the prefill benchmark")
     T = int(w.q.shape[0])
     flops = w.flops()
     peak, kind = tensor_peak()
@@ -793,6 +810,7 @@ def run_prefill(args, dev, B):
                           "frac_of_peak": round(tflops / peak, 4)},
             "step": {"us": round(t_step * 1e6, 2), "what": "kv_append of every new token + prefill attention"},
             "flops": int(flops), "new_tokens": T, "peak": peak, "peak_kind": kind, "bound": "tensor",
+            "check": {"last_rows_vs_decode_max_abs_diff": diff, "rows": int(len(has))},
             "higher_is_better": True,
             "timing": "each variant captured once as a CUDA graph, median of replays after an L2 eviction",
             "config": {"workload": f"{sp.name}: {sp.num_seqs} seqs, {sp.num_q_heads} q / {sp.num_kv_heads} kv "
