@@ -699,6 +699,13 @@ def run_op(args, rank, world, local, dist):
         B.check_swap_pairs(in_pairs, n, lay.num_blocks)
         t_out = time_it(lambda: B.swap_blocks(hk, hv, w.k_cache, w.v_cache, po, check=False), args.steps or 50)
         t_in = time_it(lambda: B.swap_blocks(dk, dv, hk, hv, pi, check=False), args.steps or 50)
+        torch.cuda.synchronize(dev)
+        src, dst = torch.from_numpy(blocks).to(dev), torch.from_numpy(back).to(dev)
+        for a_, b_ in ((dk, w.k_cache), (dv, w.v_cache)):  # the round trip is a byte copy
+            if not torch.equal(a_[dst].view(torch.uint8), b_[src].view(torch.uint8)):
+                raise RuntimeError("swap round trip is not bit-exact")
+        if B.device_error(clear=True):
+            raise RuntimeError("device error word set during the swap benchmark")
         moved = 2 * n * block_bytes
         line = {"metric": "swap_blocks GB/s (block bytes moved per direction)", "unit": "GB/s",
                 "value": round(moved / t_out / 1e9, 2),
@@ -722,6 +729,13 @@ def run_op(args, rank, world, local, dist):
         ptrs = tuple(B.layer_pointers(x) for x in (kn, vn, kc, vc))
         t_one = time_it(lambda: B.kv_append_layers(kn, vn, slots, kc, vc, ptrs=ptrs), args.steps or 50)
         t_each = time_it(lambda: [B.kv_append(kn[l], vn[l], slots, kc[l], vc[l]) for l in range(L)], args.steps or 50)
+        torch.cuda.synchronize(dev)
+        for l in (0, L // 2, L - 1):  # token t's rows sit in block t, slot 3 of every layer's cache
+            for new, cache in ((kn[l], kc[l]), (vn[l], vc[l])):
+                if not torch.equal(cache[:T, :, 3].view(torch.uint8), new.view(torch.uint8)):
+                    raise RuntimeError(f"layer {l}: appended rows differ from the new tokens")
+        if B.device_error(clear=True):
+            raise RuntimeError("device error word set during the multi-layer append benchmark")
         moved = L * T * sp.num_kv_heads * sp.head_dim * eb * 2 * 2
         line = {"metric": "kv_append over 40 layers, GB/s (read + write of the appended K/V)", "unit": "GB/s",
                 "value": round(moved / t_one / 1e9, 2),
