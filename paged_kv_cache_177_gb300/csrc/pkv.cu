@@ -161,7 +161,8 @@ int launch_bf16(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::Decod
 
 template <int D>
 int launch_f32(const pkv::DecodeParams &p, dim3 grid, cudaStream_t st, bool pdl = false) {
-    const size_t smem = (size_t)kNcw * p.group * (D + 2) * sizeof(float);
+    // every warp's per-head states, then the group's query rows
+    const size_t smem = ((size_t)kNcw * p.group * (D + 2) + (size_t)p.group * D) * sizeof(float);
     if (pdl) return launch_pdl(pkv::decode_f32_kernel<D, kNcw>, grid, dim3(kNcw * 32), smem, st, p);
     pkv::decode_f32_kernel<D, kNcw><<<grid, kNcw * 32, smem, st>>>(p);
     return check_launch();

@@ -1164,14 +1164,20 @@ struct PrefillParams {
 // K1 (fp32): same decomposition on the CUDA cores, for fp32 caches where the
 // result must hold to ~1e-5. One CTA per (partition, kv head, sequence); warp w
 // takes blocks w, w+NCW, ...; lane l owns head-dim elements l, l+32, ...
-// Each token: x = scale log2(e) <q, K_t> (warp sum), then the online update
-//   m' = max(m, x), l = l 2^(m-m') + 2^(x-m'), acc = acc 2^(m-m') + 2^(x-m') V_t.
+// Eight tokens at a time: their K and V rows stay in registers while every
+// query head of the group attends them (each K/V element read once). For one
+// head, the lanes' partial dot products of the 8 tokens are summed by a
+// transpose-reduce (9 shuffles; lane 4 t ends with token t's full sum), then
+// the online update over the 8 scores x_t = scale log2(e) <q, K_t>:
+//   m' = max(m, max_t x_t), l = l 2^(m-m') + sum_t 2^(x_t-m'),
+//   acc = acc 2^(m-m') + sum_t 2^(x_t-m') V_t.
+// Each head's (m, l, acc) lives in shared memory between passes.
 // =====================================================================================
 template <int D, int NCW>
 __global__ void __launch_bounds__(NCW * 32) decode_f32_kernel(const DecodeParams p) {
     pdl_wait();  // the caches may have been written by the previous kernel (kv_append in a decode step)
     constexpr int PER = D / 32;
-    extern __shared__ float fsm[];  // merge buffer: [NCW][g][D + 2]
+    extern __shared__ float fsm[];  // per-warp head states (also the merge buffer) [NCW][g][D + 2], q [g][D]
     const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = p.group;
@@ -1194,48 +1200,98 @@ __global__ void __launch_bounds__(NCW * 32) decode_f32_kernel(const DecodeParams
     const float *vc = static_cast<const float *>(p.v_cache);
     const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks_per_seq + b_begin;
 
+    // Per warp, every head's running state [m, l, acc[D]] lives in fsm (the merge buffer); the
+    // group's query rows sit after all warps' states. A block is taken 8 tokens at a time: their
+    // K and V rows stay in registers (lane: head-dim elements lane, lane + 32, ..) while every
+    // head of the group attends them, so each K/V element is read once.
+    float *st = fsm + (size_t)warp * g * (D + 2);
+    float *qs = fsm + (size_t)NCW * g * (D + 2);
+    for (int i = tid; i < g * D; i += NCW * 32)
+        qs[i] = __ldg(static_cast<const float *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)h * g) * D + i);
     for (int n = 0; n < g; ++n) {
-        const float *qrow = static_cast<const float *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)h * g + n) * D;
-        float qv[PER], acc[PER];
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            qv[i] = __ldg(qrow + lane + 32 * i);
-            acc[i] = 0.f;
+        for (int i = 0; i < PER; ++i) st[n * (D + 2) + 2 + lane + 32 * i] = 0.f;
+        if (lane == 0) {
+            st[n * (D + 2)] = -INFINITY;
+            st[n * (D + 2) + 1] = 0.f;
         }
-        float m = -INFINITY, l = 0.f;
-        for (int j = warp; j < nb; j += NCW) {
-            const int pb = __ldg(bt + j);
-            const bool bad = pb < 0 || pb >= p.num_blocks;
-            if (bad && lane == 0 && n == 0) raise_error(PKV_DEVERR_BLOCK_ID);
-            const int valid = (b_begin + j == nblk - 1) ? last_valid : kBlock;
-            const size_t tile = bad ? 0 : ((size_t)pb * p.num_kv_heads + h) * kBlock * D;
-            for (int t = 0; t < valid; ++t) {
-                float dot = 0.f;
-                float vv[PER];
+    }
+    __syncthreads();
+    // After the transpose-reduce below lane L holds the dot product of token tok(L) of the 8:
+    // bits 2, 3, 4 of L are bits 0, 1, 2 of the token, so lane 4 t holds token t.
+    const int tok = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+    const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
+    for (int j = warp; j < nb; j += NCW) {
+        const int pb = __ldg(bt + j);
+        const bool bad = pb < 0 || pb >= p.num_blocks;
+        if (bad && lane == 0) raise_error(PKV_DEVERR_BLOCK_ID);
+        const int valid = (b_begin + j == nblk - 1) ? last_valid : kBlock;
+        const size_t tile = bad ? 0 : ((size_t)pb * p.num_kv_heads + h) * kBlock * D;
+        for (int t0 = 0; t0 < valid; t0 += 8) {
+            float kx[8][PER], vx[8][PER];
+#pragma unroll
+            for (int tt = 0; tt < 8; ++tt)
 #pragma unroll
                 for (int i = 0; i < PER; ++i) {
-                    const float kx = bad ? 0.f : __ldg(kc + tile + (size_t)t * D + lane + 32 * i);
-                    vv[i] = bad ? 0.f : __ldg(vc + tile + (size_t)t * D + lane + 32 * i);
-                    dot = fmaf(qv[i], kx, dot);
+                    const bool in = !bad && t0 + tt < valid;
+                    kx[tt][i] = in ? __ldg(kc + tile + (size_t)(t0 + tt) * D + lane + 32 * i) : 0.f;
+                    vx[tt][i] = in ? __ldg(vc + tile + (size_t)(t0 + tt) * D + lane + 32 * i) : 0.f;
+                }
+            for (int n = 0; n < g; ++n) {
+                float *sn = st + n * (D + 2);
+                float part[8];
+#pragma unroll
+                for (int tt = 0; tt < 8; ++tt) {
+                    float d = 0.f;
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) d = fmaf(qs[n * D + lane + 32 * i], kx[tt][i], d);
+                    part[tt] = d;
+                }
+                // transpose-reduce: 8 partial sums per lane -> one full sum per lane (9 shuffles)
+                float w4[4], w2[2];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float mine = b4 ? part[4 + k] : part[k], other = b4 ? part[k] : part[4 + k];
+                    w4[k] = mine + __shfl_xor_sync(0xffffffffu, other, 16);
                 }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                const float x = dot * p.scale_log2;
-                const float mn = fmaxf(m, x);
-                const float al = exp2f(m - mn);
-                const float pw = exp2f(x - mn);
-                l = l * al + pw;
+                for (int k = 0; k < 2; ++k) {
+                    const float mine = b3 ? w4[2 + k] : w4[k], other = b3 ? w4[k] : w4[2 + k];
+                    w2[k] = mine + __shfl_xor_sync(0xffffffffu, other, 8);
+                }
+                float dot = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
+                dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+                dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                const float x = (t0 + tok < valid) ? dot * p.scale_log2 : -INFINITY;
+                float mx = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float m_old = sn[0], l_old = sn[1];
+                const float m_new = fmaxf(m_old, mx);  // finite: the 8 hold at least one token
+                const float al = exp2f(m_old - m_new);
+                const float pw = exp2f(x - m_new);
+                float ps = pw;  // the 8 weights' sum (each token once: reduce over bits 2-4 only)
+                ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+                float acc[PER];
 #pragma unroll
-                for (int i = 0; i < PER; ++i) acc[i] = fmaf(acc[i], al, pw * vv[i]);
-                m = mn;
+                for (int i = 0; i < PER; ++i) acc[i] = sn[2 + lane + 32 * i] * al;
+#pragma unroll
+                for (int tt = 0; tt < 8; ++tt) {
+                    const float pt = __shfl_sync(0xffffffffu, pw, 4 * tt);
+#pragma unroll
+                    for (int i = 0; i < PER; ++i) acc[i] = fmaf(pt, vx[tt][i], acc[i]);
+                }
+                __syncwarp();  // every lane has read sn before it is overwritten
+#pragma unroll
+                for (int i = 0; i < PER; ++i) sn[2 + lane + 32 * i] = acc[i];
+                if (lane == 0) {
+                    sn[0] = m_new;
+                    sn[1] = l_old * al + ps;
+                }
+                __syncwarp();
             }
-        }
-        float *row = fsm + ((size_t)warp * g + n) * (D + 2);
-#pragma unroll
-        for (int i = 0; i < PER; ++i) row[2 + lane + 32 * i] = acc[i];
-        if (lane == 0) {
-            row[0] = m;
-            row[1] = l;
         }
     }
     __syncthreads();

@@ -61,6 +61,8 @@ CASES = [
     ("gqa12_d64", "bf16", 12, 1, 64),
     ("f32_gqa4_d128", "f32", 8, 2, 128),
     ("f32_gqa16_d64", "f32", 16, 1, 64),
+    ("f32_mha_d128", "f32", 4, 4, 128),
+    ("f32_gqa8_d128", "f32", 16, 2, 128),
 ]
 
 
@@ -241,6 +243,22 @@ def test_full_size_workload(name):
     assert torch.isfinite(o).all()
     vmax = torch.nan_to_num(w.v_cache.float(), nan=0.0).abs().max()
     assert float(o.abs().max()) <= float(vmax) * (1 + 1e-2)
+
+
+@pytest.mark.parametrize("name", ["mha13b", "gqa8b", "long_context"])
+def test_full_size_fp32(name):
+    """The 13B-class, GQA and long-context batches with fp32 caches (the
+    CUDA-core path): sampled sequences against the oracle at the fp32 bound."""
+    w = W.make_workload(name, device="cuda", dtype="f32")
+    lay = w.layout
+    h = H.host_arrays(w)
+    out = H.gpu_step(w, lay.spec.partition_tokens)
+    torch.cuda.synchronize()
+    order = np.argsort(lay.context_lens, kind="stable")
+    pick = sorted({int(order[-1]), int(order[0]), int(order[len(order) // 2])})
+    ref = H.oracle_step(h, lay, w.scale, seq_ids=pick)
+    H.assert_close(out[torch.as_tensor(pick, device="cuda")], ref, "f32", f"{name} fp32")
+    assert torch.isfinite(out).all()
 
 
 def test_persistent_path_leaves_counters_zero_and_repeats_bit_identically():
