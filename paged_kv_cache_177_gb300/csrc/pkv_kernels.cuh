@@ -1173,8 +1173,10 @@ struct PrefillParams {
 //   acc = acc 2^(m-m') + sum_t 2^(x_t-m') V_t.
 // Each head's (m, l, acc) lives in shared memory between passes.
 // =====================================================================================
+// Five CTAs per SM (at most 96 registers per thread, no spills): more warps hide more of
+// the load latency (measured: GQA batches 5-9% faster, 13B-class MHA within 1%).
 template <int D, int NCW>
-__global__ void __launch_bounds__(NCW * 32) decode_f32_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(NCW * 32, 5) decode_f32_kernel(const DecodeParams p) {
     pdl_wait();  // the caches may have been written by the previous kernel (kv_append in a decode step)
     constexpr int PER = D / 32;
     extern __shared__ float fsm[];  // per-warp head states (also the merge buffer) [NCW][g][D + 2], q [g][D]
