@@ -22,7 +22,6 @@ tables and context lengths of the running batch.
 """
 from __future__ import annotations
 
-import heapq
 from collections import deque
 from dataclasses import dataclass, field
 from typing import Deque, Dict, List, Optional, Sequence, Tuple
@@ -32,44 +31,46 @@ import numpy as np
 from .block_manager import BlockManager, NoFreeBlocks, blocks_needed
 
 
+def slot_simulation(output_lengths: Sequence[int], slots: int, continuous: bool) -> List[float]:
+    """Runs requests (each needing ``output_lengths[i]`` decode steps, in queue
+    order) on ``slots`` slots, one decode step per loop iteration, and returns
+    the fraction of busy slots at every step. Static batching admits the next
+    ``slots`` requests only once every slot is idle; continuous batching
+    refills any idle slot before each step."""
+    queue = deque(output_lengths)
+    left = [0] * slots                       # decode steps each slot's request still needs
+    busy: List[float] = []
+    while queue or any(left):
+        if continuous or not any(left):
+            for i in range(slots):
+                if left[i] == 0 and queue:
+                    left[i] = queue.popleft()
+        if not any(left):                    # only zero-length requests were admitted
+            continue
+        busy.append(sum(1 for n in left if n > 0) / slots)
+        left = [n - 1 if n > 0 else 0 for n in left]
+    return busy
+
+
 def static_batching(output_lengths: Sequence[int], slots: int) -> Tuple[int, float]:
-    """Decode steps and slot occupancy when each group of ``slots`` requests
-    (in arrival order) runs until its longest member finishes."""
-    lengths = list(output_lengths)
-    steps = sum(max(lengths[i:i + slots]) for i in range(0, len(lengths), slots))
-    return steps, sum(lengths) / (steps * slots)
+    """Decode steps and mean slot occupancy when each group of ``slots``
+    requests runs until its longest member finishes."""
+    busy = slot_simulation(output_lengths, slots, continuous=False)
+    return len(busy), sum(busy) / max(len(busy), 1)
 
 
 def continuous_batching(output_lengths: Sequence[int], slots: int) -> Tuple[int, float]:
-    """Decode steps and slot occupancy when each queued request starts in the
-    first slot that frees up (a min-heap of the slots' free times)."""
-    free_at = [0] * slots
-    heapq.heapify(free_at)
-    for n in output_lengths:
-        start = heapq.heappop(free_at)
-        heapq.heappush(free_at, start + n)
-    steps = max(free_at)
-    return steps, sum(output_lengths) / (steps * slots)
+    """Decode steps and mean slot occupancy when a queued request takes any
+    slot that is idle at the start of a step."""
+    busy = slot_simulation(output_lengths, slots, continuous=True)
+    return len(busy), sum(busy) / max(len(busy), 1)
 
 
 def utilisation_traces(output_lengths: Sequence[int], slots: int) -> Tuple[List[float], List[float]]:
     """Per-step fraction of busy slots for static and continuous batching
     (queue order), without padding either trace to the other's length."""
-    lengths = list(output_lengths)
-    static = []
-    for i in range(0, len(lengths), slots):
-        batch = lengths[i:i + slots]
-        for step in range(max(batch)):
-            static.append(sum(1 for n in batch if step < n) / slots)
-    cont = []
-    queue = deque(lengths)
-    active: List[int] = []
-    while active or queue:
-        while len(active) < slots and queue:
-            active.append(queue.popleft())
-        cont.append(len(active) / slots)
-        active = [r - 1 for r in active if r > 1]
-    return static, cont
+    return (slot_simulation(output_lengths, slots, continuous=False),
+            slot_simulation(output_lengths, slots, continuous=True))
 
 
 @dataclass
