@@ -16,8 +16,14 @@ HBM.  ``e2e`` repeats the measurement with the per-step inputs in pinned host
 memory and the output going back there, inside the timed region: through the
 copy engine, and in place (the kernels read and write the pinned host
 buffers over NVLink-C2C); the faster is reported, both are shown.
-``parity`` compares the timed step's output with the oracle on a few
-sequences of the batch.
+``parity`` compares the timed step's output with the oracle on every
+sequence and head of the batch, and reports the error of the same call with
+fp32 output (the accumulator before bf16 rounding) against 2e-3 alone.
+Without ``--workload`` the line headlines mha13b (the 13B-class batch) and
+adds a ``configs`` object: every other configuration of the workload set
+(tiny, gqa8b, parallel_sampling, long_context) timed the same way (step and
+attention call), checked against the oracle on every sequence, and with the
+oracle's own rate on the host cores.
 Under torchrun every rank runs its own replica of the workload (weak
 scaling): the path has no exchange step.
 """
@@ -263,22 +269,132 @@ def oracle_sample(lay: W.Layout, host: dict, target_s: float, nthreads: int = 0)
     return nbytes * passes / total / 1e9, total, int(n), passes, nbytes
 
 
-def sampled_parity(lay: W.Layout, host: dict, out: torch.Tensor, dtype: str, n: int = 8):
-    """The timed step's output against the oracle on ``n`` sequences spread over
-    the batch (the host caches already hold the step's copies and appends)."""
+def full_parity(lay: W.Layout, host: dict, out: torch.Tensor, dtype: str, out32=None):
+    """The timed step's output against the oracle on every sequence and head
+    (the host caches already hold the step's copies and appends). ``out32``:
+    the same attention call with fp32 output (bf16 inputs), whose error before
+    rounding is reported against 2e-3 absolute alone."""
     import oracle
 
-    ids = np.unique(np.linspace(0, lay.spec.num_seqs - 1, n).astype(np.int64))
     ref = oracle.paged_decode_attention(host["q"], host["k_cache"], host["v_cache"], lay.block_tables,
                                         lay.context_lens, 1.0 / math.sqrt(lay.spec.head_dim), lay.spec.num_kv_heads,
-                                        seq_ids=ids, nthreads=cpu_cores())
-    got = out[torch.from_numpy(ids).to(out.device)].float().cpu().numpy().astype(np.float64)
+                                        nthreads=cpu_cores())
+    got = out.float().cpu().numpy().astype(np.float64)
     err = np.abs(got - ref)
     atol, rtol = (2e-3, 1e-2) if dtype == "bf16" else (1e-5, 1e-5)
-    return {"sample_seqs": int(len(ids)), "max_abs_err": float(err.max()),
-            "max_rel_err": float((err / np.maximum(np.abs(ref), 1e-30)).max()),
-            "bound": f"|gpu - ref| <= {atol:g} + {rtol:g} |ref| per element",
-            "within_bound": bool(np.all(err <= atol + rtol * np.abs(ref)))}
+    res = {"sample_seqs": int(lay.spec.num_seqs), "of_seqs": int(lay.spec.num_seqs), "elements": int(err.size),
+           "max_abs_err": float(err.max()),
+           "max_rel_err": float((err / np.maximum(np.abs(ref), 1e-30)).max()),
+           "bound": f"|gpu - ref| <= {atol:g} + {rtol:g} |ref| per element",
+           "within_bound": bool(np.all(np.isfinite(got)) and np.all(err <= atol + rtol * np.abs(ref)))}
+    if out32 is not None:
+        g32 = out32.cpu().numpy().astype(np.float64)
+        e32 = np.abs(g32 - ref)
+        res["unrounded"] = {
+            "max_abs_err": float(e32.max()), "bound": "2e-3 absolute",
+            "within_bound": bool(np.all(np.isfinite(g32)) and e32.max() <= 2e-3),
+            "rounds_to_output": bool(torch.equal(out32.to(torch.bfloat16).cpu().view(torch.int16),
+                                                 out.cpu().view(torch.int16))),
+            "how": "the same attention call with fp32 output (PKV_BF16_OUT_F32): O / L before rounding to bf16"}
+    return res
+
+
+def unrounded_output(B, w, lay, pt, ws, stream):
+    """fp32 output of the attention call on bf16 inputs, or None for fp32."""
+    if w.q.dtype != torch.bfloat16:
+        return None
+    out32 = torch.empty(tuple(w.q.shape), dtype=torch.float32, device=w.q.device)
+    B.paged_decode_attention(out32, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
+                             max_context_len=lay.max_context_len, partition_tokens=pt, workspace=ws, stream=stream)
+    return out32
+
+
+def config_summary(name: str, args, dev, B, evict) -> dict:
+    """One more workload in the default run: its decode step (one
+    paged_decode_step, replayed as a CUDA graph, L2 evicted between steps) and
+    the attention call alone, timed with CUDA events; its output against the
+    oracle on every sequence; and the oracle's rate on the host cores."""
+    sp = W.spec(name)
+    pt = sp.partition_tokens
+    w = W.make_workload(sp, device=dev)
+    lay = w.layout
+    S, Hq, Hkv, D = sp.num_seqs, sp.num_q_heads, sp.num_kv_heads, sp.head_dim
+    maxlen = lay.max_context_len
+    nbytes = step_bytes(lay)
+    ws = torch.zeros(max(B.workspace_bytes(S, Hq, Hkv, D, maxlen, pt), 16), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(w.q)
+    stream = torch.cuda.Stream(dev)
+    has_pairs = len(lay.cow_pairs) > 0
+    persistent = B.decode_persistent(S, Hkv, pt, w.q.dtype)
+    launches = B.decode_launches(S, Hkv, maxlen, pt, w.q.dtype)
+    B.check_copy_pairs(lay.cow_pairs, lay.num_blocks)
+
+    def step():
+        B.paged_decode_step(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, w.k_new,
+                            w.v_new, w.slot_mapping, w.cow_pairs if has_pairs else None, check=False,
+                            max_context_len=maxlen, partition_tokens=pt, workspace=ws, stream=stream)
+
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            evict.sum()
+            step()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    n = args.config_steps
+    attn_args = B.decode_args(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
+                              max_context_len=maxlen, partition_tokens=pt, workspace=ws, stream=stream)
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    aev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            evict.sum()
+            sev[i][0].record(stream)
+            g.replay()
+            sev[i][1].record(stream)
+        for i in range(n):
+            evict.sum()
+            aev[i][0].record(stream)
+            B.decode_raw(attn_args)
+            aev[i][1].record(stream)
+        out32 = unrounded_output(B, w, lay, pt, ws, stream)
+    torch.cuda.synchronize(dev)
+    err = B.device_error(clear=True)
+    if err:
+        raise RuntimeError(f"{name}: device error word set: {err:#x}")
+    step_ms = sorted(a.elapsed_time(b) for a, b in sev)
+    attn_ms = [a.elapsed_time(b) for a, b in aev]
+    t_step = sum(step_ms) / n / 1e3
+    t_attn = sum(attn_ms) / n / 1e3
+    peak, _ = peaks()
+    host = {k: W.to_numpy(getattr(w, k)) for k in ("q", "k_cache", "v_cache", "k_new", "v_new")}
+    gbs, secs, nseq, passes, sb = oracle_sample(lay, host, args.config_cpu_seconds)
+    parity = full_parity(lay, host, out, sp.dtype, out32)
+    kernel = ("decode_bf16_persistent_kernel" if persistent else
+              ("decode_bf16_kernel" if sp.dtype == "bf16" else "decode_f32_kernel") +
+              (" + lse_reduce_kernel" if launches == 2 else ""))
+    res = {
+        "workload": describe(sp),
+        "partition_tokens": "balanced (persistent kernel)" if persistent else B.partition_tokens(S, Hkv, maxlen, pt),
+        "us_per_step": round(t_step * 1e6, 2),
+        "us_per_step_p10_p90": [round(step_ms[n // 10] * 1e3, 2), round(step_ms[(9 * n) // 10] * 1e3, 2)],
+        "step_GBps": round(nbytes["total"] / t_step / 1e9, 2),
+        "seqs_per_s": round(S / t_step, 1),
+        "attention": {"kernel": kernel, "us": round(t_attn * 1e6, 2),
+                      "GBps": round(nbytes["attention"] / t_attn / 1e9, 2),
+                      "roofline_frac": round(nbytes["attention"] / t_attn / 1e9 / peak, 4),
+                      "bytes_per_launch": nbytes["attention"]},
+        "step_bytes": nbytes,
+        "timed_steps": n,
+        "parity": parity,
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{nseq} of {S} sequences ({sb / 1e6:.1f} MB of K/V, all heads) x {passes} "
+                                   f"passes in {secs:.1f} s"},
+    }
+    del w, ws, out, g
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_reference(args, rank, world, dist):
@@ -529,7 +645,20 @@ def run_ours(args, rank, world, local, dist):
         g1, s1, n1, p1, b1 = oracle_sample(lay, host, min(3.0, args.cpu_seconds / 3), nthreads=1)
         cpu["single_thread"] = {"value": round(g1, 4), "unit": "GB/s", "cores": 1,
                                 "sample": f"{n1} sequences ({b1 / 1e6:.1f} MB) x {p1} passes in {s1:.1f} s"}
-        parity = sampled_parity(lay, host, out, sp.dtype)
+        out32 = unrounded_output(B, w, lay, pt, ws, stream)
+        torch.cuda.synchronize(dev)
+        parity = full_parity(lay, host, out, sp.dtype, out32)
+    configs = None
+    if world == 1 and args.all_configs:
+        # the other configurations of the workload set, each measured and
+        # checked the same way (the headline's buffers are released first)
+        del g_step, g_zc
+        torch.cuda.empty_cache()
+        configs = {name: config_summary(name, args, dev, B, evict)
+                   for name in W.CONFIG_ORDER if name != sp.name}
+        configs["all_within_bound"] = bool(
+            (parity is None or parity["within_bound"]) and
+            all(c["parity"]["within_bound"] for c in configs.values() if isinstance(c, dict)))
     srt = sorted(step_ms)
     roof_kernel = "decode_bf16_persistent_kernel" if persistent else "decode_bf16_kernel"
     # the captures were taken on the workloads' default launch configuration
@@ -586,6 +715,7 @@ def run_ours(args, rank, world, local, dist):
         "cpu_baseline": cpu,
         "parity": parity,
         "wall_s_timed_region": round(wall, 3),
+        "configs": configs,
     }
     print(json.dumps(line), flush=True)
 
@@ -841,7 +971,13 @@ def main():
                     help="timed steps (default: enough for about 1.5 s of device time)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mha13b", choices=list(W.SPECS))
+    ap.add_argument("--workload", default=None, choices=list(W.SPECS),
+                    help="the workload to time (default mha13b, the headline, followed by every other "
+                         "configuration in a 'configs' object)")
+    ap.add_argument("--config-steps", type=int, default=300, help="timed steps per extra configuration")
+    ap.add_argument("--config-cpu-seconds", type=float, default=3.0,
+                    help="oracle seconds per extra configuration's cpu_baseline")
+    ap.add_argument("--no-configs", action="store_true", help="time the headline workload only")
     ap.add_argument("--partition-tokens", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
@@ -854,6 +990,9 @@ def main():
         ap.error("at least 3 warm-up steps")
     if args.impl == "reference" and args.steps is None:
         args.steps = 5
+    args.all_configs = args.workload is None and not args.no_configs and args.partition_tokens is None
+    if args.workload is None:
+        args.workload = "mha13b"
     rank, world, local, dist = dist_setup(args)
     if args.gpus != world and world > 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)

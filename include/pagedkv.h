@@ -42,6 +42,12 @@
  *    [num_tokens][num_kv_heads][head_dim]. All row-major, contiguous.
  *  - dtype: PKV_BF16 (bf16 storage, fp32 accumulation, bf16 output rounded to
  *    nearest even) or PKV_F32 (fp32 throughout). q, caches and out share it.
+ *    The decode calls (paged_decode_attention, paged_decode_step,
+ *    paged_decode_attention_static_workspace and the planning queries) also
+ *    take PKV_BF16_OUT_F32: bf16 q and caches, the bf16 arithmetic unchanged,
+ *    and out fp32 -- the accumulated O / L before it would be rounded to bf16,
+ *    so the kernel's own error can be measured apart from the output rounding
+ *    (append and copy inside paged_decode_step move bf16).
  *  - head_dim is 64 or 128; num_q_heads is a multiple of num_kv_heads and the
  *    group size g = num_q_heads / num_kv_heads is at most 16. Query head hq
  *    reads kv head hq / g (consecutive grouping).
@@ -67,7 +73,7 @@
 extern "C" {
 #endif
 
-typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_BF16_OUT_F32 = 2 } pkv_dtype;
 
 #define PKV_OK 0
 #define PKV_ERR_ARG -1          /* bad scalar argument, null pointer, shape mismatch */
@@ -131,13 +137,28 @@ int pkv_decode_launches(int num_seqs, int num_kv_heads, int max_context_len, int
 int pkv_decode_persistent(int num_seqs, int num_kv_heads, int partition_tokens, pkv_dtype dtype);
 
 /*
+ * Layout of every decode workspace (paged_decode_attention, paged_decode_step,
+ * paged_decode_attention_shared_prefix, and the library's own array behind
+ * paged_decode_attention_static_workspace): the first PKV_DECODE_COUNTER_BYTES
+ * bytes hold the persistent kernel's arrival counters, then come partial
+ * softmax states (max in the log2 domain, sum, partial output, fp32).
+ *  - The counters must be zero before the first call that uses the buffer
+ *    (zero-fill it once after allocating it, e.g. cudaMemsetAsync). Every
+ *    call that completes without a device error leaves them zero, and no
+ *    decode path writes anything else into them.
+ *  - The partial states need no initial value: a call writes every state it
+ *    reads earlier in the same call.
+ * So one buffer, sized for the largest call, serves calls of any shape on any
+ * decode path in turn (split grid, persistent, shared prefix), with no
+ * clearing between them. After a call that raised PKV_DEVERR_TIMEOUT, zero
+ * the counters again.
+ */
+#define PKV_DECODE_COUNTER_BYTES 10240u
+
+/*
  * Bytes of device workspace paged_decode_attention needs with these
- * arguments (0 when it needs none). The workspace holds per-sequence arrival
- * counters and partial softmax states (max in the log2 domain, sum, partial
- * output, fp32). It must be zero-filled before the first call that uses it
- * (for example cudaMemsetAsync once after allocating it); every call that
- * completes without a device error leaves it zero-filled again, so it can be
- * reused call after call without clearing.
+ * arguments (0 when it needs none): the counter header and the partial
+ * states, laid out as above.
  */
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                   int max_context_len, int partition_tokens);
@@ -154,9 +175,9 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
  *   launch); longer lengths are clamped and flagged (PKV_DEVERR_LENGTH).
  * A context length of 0 yields a zero output row.
  * workspace / workspace_bytes: device scratch of at least
- *   pkv_decode_workspace_bytes(...) bytes, zero-filled before its first use
- *   (may be NULL when that size is 0). Concurrent calls must not share a
- *   workspace. After a call that raised PKV_DEVERR_TIMEOUT, zero it again.
+ *   pkv_decode_workspace_bytes(...) bytes, laid out and initialised as
+ *   described above PKV_DECODE_COUNTER_BYTES (may be NULL when that size is
+ *   0). Concurrent calls must not share a workspace.
  * q, out, block_tables and context_lens may point to page-locked host memory
  *   (mapped into the device's address space, as cudaHostAlloc gives): the
  *   kernels read and write them in place over the host link. The caches and
@@ -213,8 +234,9 @@ int paged_decode_step(void *out, const void *q, void *k_cache, void *v_cache, co
  *   table; the caller guarantees the members agree on them.
  * group_size x (num_q_heads / num_kv_heads) must be at most 16. bf16 only.
  * Partitions of partition_tokens split each group's union of blocks.
- * workspace: at least pkv_shared_prefix_workspace_bytes(...) bytes (no
- *   zero-fill needed). partition_tokens as for paged_decode_attention (> 0 or
+ * workspace: at least pkv_shared_prefix_workspace_bytes(...) bytes; it
+ *   needs no zero-fill of its own and may be the buffer other decode calls
+ *   use (it never writes the counter header). partition_tokens as for paged_decode_attention (> 0 or
  *   0 for 512). Two launches: the prefix/suffix kernel and a merge kernel.
  */
 int paged_decode_attention_shared_prefix(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -225,7 +247,8 @@ int paged_decode_attention_shared_prefix(void *out, const void *q, const void *k
                                          int group_size, pkv_dtype dtype, int partition_tokens, void *workspace,
                                          size_t workspace_bytes, void *stream);
 
-/* Workspace bytes paged_decode_attention_shared_prefix needs. */
+/* Workspace bytes paged_decode_attention_shared_prefix needs (the decode
+ * workspace layout above: its counter header is left untouched). */
 size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
                                          int group_size, int partition_tokens);
 
@@ -383,11 +406,15 @@ int pkv_device_error(uint32_t *value, int clear);
  *
  * The first call on a device looks up the array's device address with that
  * device current and caches it; make that first call before any stream
- * capture. All calls share the one array and it keeps the last call's
- * contents; nothing else in it needs to start at zero, because every partial
- * result a call reads was written earlier by the same call, and the arrival
- * counters it uses start at zero when the library loads and are left at zero
- * by every call that completes without a device error. Calls that
+ * capture. All calls share the one array, laid out like any decode
+ * workspace (see PKV_DECODE_COUNTER_BYTES), and it keeps the last call's
+ * contents: its counter header starts at zero when the library loads and
+ * every call that completes without a device error leaves it zero, whatever
+ * path (persistent or split grid) and shape the calls before it took; the
+ * partial states after it need no clearing, because a call writes every state
+ * it reads. After a call that raised PKV_DEVERR_TIMEOUT the header may hold
+ * stale counts: no entry point clears it, so such a process should stop
+ * using this call. Calls that
  * overlap on the GPU (different streams, or different host threads, without
  * ordering between them) race on the array: order them, or use
  * paged_decode_attention with separate workspaces.

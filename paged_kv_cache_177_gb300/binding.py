@@ -23,11 +23,13 @@ if not os.path.exists(LIB):
 
 _lib = ctypes.CDLL(LIB)
 
-PKV_F32, PKV_BF16 = 0, 1
+PKV_F32, PKV_BF16, PKV_BF16_OUT_F32 = 0, 1, 2
 PARTITION_AUTO, PARTITION_BALANCED = 0, -1
 DEVERR_BLOCK_ID, DEVERR_SLOT, DEVERR_PAIR, DEVERR_TIMEOUT, DEVERR_LENGTH = 0x1, 0x2, 0x4, 0x8, 0x10
 DEVERR_POINTER = 0x20
 BLOCK_SIZE = 16
+# the arrival counters at the head of every decode workspace (PKV_DECODE_COUNTER_BYTES)
+DECODE_COUNTER_BYTES = 10240
 
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 
@@ -164,8 +166,12 @@ def decode_args(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cac
     (see there) into the C-ABI argument tuple, for ``decode_raw``."""
     dev = _dev_io([k_cache, v_cache], [out, q, block_tables, context_lens])
     dt = _dtype_code(q)
-    if not (out.dtype == q.dtype == k_cache.dtype == v_cache.dtype):
-        raise TypeError("q, out and the caches must share one dtype")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("q and the caches must share one dtype")
+    if out.dtype != q.dtype:
+        if not (q.dtype == torch.bfloat16 and out.dtype == torch.float32):
+            raise TypeError("out must have q's dtype, or be fp32 with bf16 q (the unrounded accumulator)")
+        dt = PKV_BF16_OUT_F32
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise TypeError("block_tables and context_lens must be int32")
     S, Hq, D = q.shape
@@ -205,12 +211,17 @@ def paged_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
 
     q, out: [S, Hq, D]; k_cache, v_cache: [NB, Hkv, 16, D] (bf16 or fp32,
     all one dtype); block_tables int32 [S, maxB]; context_lens int32 [S].
+    With bf16 q and caches, ``out`` may be fp32: it then receives the
+    accumulated O / L before rounding to bf16 (PKV_BF16_OUT_F32), the same
+    arithmetic otherwise.
     ``max_context_len`` defaults to context_lens.max() (a device sync).
     ``partition_tokens``: 0 automatic, -1 balanced (persistent kernel, bf16),
     > 0 fixed partitions of that many tokens.
     A caller-provided ``workspace`` must have been zero-filled once before
-    its first use; the library leaves the part that must start at zero at
-    zero after each call, so it is reused without clearing.
+    its first use; its counter header (the first DECODE_COUNTER_BYTES) is
+    left zero after each call and no decode path writes anything else there,
+    so one workspace sized for the largest call serves every call and path
+    without clearing.
     q, out, block_tables and context_lens may be pinned host tensors: the
     kernels then read and write them in place (no separate copy).
     """

@@ -37,7 +37,11 @@ constexpr int kMaxParts = 8192;        // partitions per sequence the reduce ker
 #ifndef PKV_PERSIST_STAGES_D64
 #define PKV_PERSIST_STAGES_D64 2
 #endif
+#ifndef PKV_MHA_CUDA_CORES
+#define PKV_MHA_CUDA_CORES 1
+#endif
 constexpr int kNstage = PKV_GRID_STAGES;
+constexpr bool kMhaCudaCores = PKV_MHA_CUDA_CORES != 0;  // g = 1 on the CUDA cores (persistent kernel)
 
 constexpr int kNcw = PKV_GRID_CONSUMERS;
 // persistent bf16 kernel: one CTA of kPersistWarps warps per SM
@@ -54,6 +58,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int elem_bytes(pkv_dtype dt) { return dt == PKV_BF16 ? 2 : 4; }
 
 bool dtype_ok(pkv_dtype dt) { return dt == PKV_BF16 || dt == PKV_F32; }
+
+// The storage type of q and the caches for a decode dtype (PKV_BF16_OUT_F32
+// reads bf16 and writes fp32).
+pkv_dtype input_dtype(pkv_dtype dt) { return dt == PKV_BF16_OUT_F32 ? PKV_BF16 : dt; }
 
 int check_launch() {
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -141,11 +149,11 @@ int max_parts_for(int max_context_len, int part_tokens) {
     return (max_context_len + part_tokens - 1) / part_tokens;
 }
 
-template <int D, int NT>
+template <int D, int NT, typename OutT>
 int launch_bf16(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, dim3 grid,
                 cudaStream_t st, bool pdl = false) {
     using C = pkv::Bf16Cfg<D, NT, kNstage, kNcw>;
-    auto kern = pkv::decode_bf16_kernel<D, NT, kNstage, kNcw>;
+    auto kern = pkv::decode_bf16_kernel<D, NT, kNstage, kNcw, OutT>;
     static thread_local int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -227,20 +235,26 @@ int launch_prefill_tc(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUte
 }
 
 
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+// Every decode workspace starts with the persistent kernel's arrival counters
+// (one per worker, zero between calls); no path writes anything else there,
+// so one buffer serves every decode path and shape in turn. Partial softmax
+// states follow; each call writes them before it reads them.
+constexpr size_t kCounterBytes = PKV_DECODE_COUNTER_BYTES;
+static_assert((size_t)kPersistMaxCtas * kPersistWarps * sizeof(int) <= kCounterBytes,
+              "one arrival counter per persistent worker");
+static_assert(kCounterBytes % 256 == 0, "partials start 256-byte aligned");
 
 size_t grid_workspace_bytes(int num_seqs, int num_q_heads, int head_dim, int max_context_len, int pt) {
     const int mp = max_parts_for(max_context_len, pt);
     if (mp <= 1) return 0;
-    return (size_t)num_seqs * num_q_heads * mp * (2 + (size_t)head_dim) * sizeof(float);
+    return kCounterBytes + (size_t)num_seqs * num_q_heads * mp * (2 + (size_t)head_dim) * sizeof(float);
 }
 
-// Arrival counters [S][Hkv] (zero between calls), then one (max, sum, acc)
-// state per group head for up to two cut segments per warp.
-size_t persist_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
+// The counters, then one (max, sum, acc) state per group head for up to two
+// cut segments per worker.
+size_t persist_workspace_bytes(int num_q_heads, int num_kv_heads, int head_dim) {
     const int g = num_q_heads / num_kv_heads;
-    return align256((size_t)num_seqs * num_kv_heads * sizeof(int)) +
-           (size_t)kPersistMaxCtas * kPersistWarps * 2 * g * (2 + (size_t)head_dim) * sizeof(float);
+    return kCounterBytes + (size_t)kPersistMaxCtas * kPersistWarps * 2 * g * (2 + (size_t)head_dim) * sizeof(float);
 }
 
 int sm_count(int *n) {
@@ -258,12 +272,12 @@ int sm_count(int *n) {
     return PKV_OK;
 }
 
-template <int D, int NT, int NS, int NW>
+template <int D, int NT, int NS, int NW, typename OutT, class WA = pkv::WarpAttn<D, NT>>
 int launch_persistent(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, cudaStream_t st,
                       bool pdl = false) {
     using C = pkv::PersistCfg<D, NT, NS, NW>;
     static_assert(C::smem_bytes(kPersistMaxSeqs) + 64 <= kSmemLimit, "persistent kernel exceeds shared memory");
-    auto kern = pkv::decode_bf16_persistent_kernel<D, NT, NS, NW>;
+    auto kern = pkv::decode_bf16_persistent_kernel<D, NT, NS, NW, OutT, WA>;
     static thread_local int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -279,6 +293,37 @@ int launch_persistent(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv:
     if (pdl) return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::smem_bytes(p.num_seqs), st, tmk, tmv, p);
     kern<<<grid, C::kThreads, C::smem_bytes(p.num_seqs), st>>>(tmk, tmv, p);
     return check_launch();
+}
+
+// Head-dim and group-width dispatch of the two bf16 decode kernels: groups
+// wider than 8 need two MMA column tiles (the persistent kernel then runs
+// half the warps with twice the stages, so their registers fit unspilled).
+// One query head per kv head (g = 1) takes the CUDA-core step: the block's
+// contraction is then a matrix-vector product that would fill one of the
+// tensor cores' eight MMA columns.
+template <typename OutT, int NS128, int NS64, int NW>
+int persistent_by_shape(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, cudaStream_t st,
+                        bool pdl, int head_dim, int g) {
+    if (head_dim == 128) {
+        if (g == 1 && kMhaCudaCores)
+            return launch_persistent<128, 1, NS128, NW, OutT, pkv::WarpAttnScalar<128>>(tmk, tmv, p, st, pdl);
+        return g <= 8 ? launch_persistent<128, 1, NS128, NW, OutT>(tmk, tmv, p, st, pdl)
+                      : launch_persistent<128, 2, 2 * NS128, NW / 2, OutT>(tmk, tmv, p, st, pdl);
+    }
+    if (g == 1 && kMhaCudaCores)
+        return launch_persistent<64, 1, NS64, NW, OutT, pkv::WarpAttnScalar<64>>(tmk, tmv, p, st, pdl);
+    return g <= 8 ? launch_persistent<64, 1, NS64, NW, OutT>(tmk, tmv, p, st, pdl)
+                  : launch_persistent<64, 2, 2 * NS64, NW / 2, OutT>(tmk, tmv, p, st, pdl);
+}
+
+template <typename OutT>
+int grid_by_shape(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, dim3 grid,
+                  cudaStream_t st, bool pdl, int head_dim, int g) {
+    if (head_dim == 128)
+        return g <= 8 ? launch_bf16<128, 1, OutT>(tmk, tmv, p, grid, st, pdl)
+                      : launch_bf16<128, 2, OutT>(tmk, tmv, p, grid, st, pdl);
+    return g <= 8 ? launch_bf16<64, 1, OutT>(tmk, tmv, p, grid, st, pdl)
+                  : launch_bf16<64, 2, OutT>(tmk, tmv, p, grid, st, pdl);
 }
 
 // The persistent balanced kernel is chosen for bf16 when asked for
@@ -342,19 +387,19 @@ size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_head
     if (pt <= 0 || pt % 16 != 0) return 0;
     const size_t grid_ws = grid_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, pt);
     if (partition_tokens > 0 || num_q_heads % num_kv_heads != 0) return grid_ws;
-    const size_t pers = persist_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim);
+    const size_t pers = persist_workspace_bytes(num_q_heads, num_kv_heads, head_dim);
     return pers > grid_ws ? pers : grid_ws;
 }
 
 int pkv_decode_persistent(int num_seqs, int num_kv_heads, int partition_tokens, pkv_dtype dtype) {
     if (num_seqs <= 0 || num_kv_heads <= 0 || partition_tokens < PKV_PARTITION_BALANCED) return 0;
-    return use_persistent(dtype, partition_tokens, num_seqs, num_kv_heads) ? 1 : 0;
+    return use_persistent(input_dtype(dtype), partition_tokens, num_seqs, num_kv_heads) ? 1 : 0;
 }
 
 int pkv_decode_launches(int num_seqs, int num_kv_heads, int max_context_len, int partition_tokens, pkv_dtype dtype) {
     if (num_seqs <= 0 || num_kv_heads <= 0) return 0;
     if (partition_tokens < PKV_PARTITION_BALANCED) return 0;
-    if (use_persistent(dtype, partition_tokens, num_seqs, num_kv_heads)) return 1;
+    if (use_persistent(input_dtype(dtype), partition_tokens, num_seqs, num_kv_heads)) return 1;
     const int pt = pkv_decode_partition_tokens(num_seqs, 1, max_context_len, partition_tokens);
     if (pt <= 0 || pt % 16 != 0) return 0;
     return max_parts_for(max_context_len, pt) > 1 ? 2 : 1;
@@ -525,8 +570,10 @@ size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int head
     const int pt = pkv_decode_partition_tokens(num_seqs, 1, max_context_len, partition_tokens);
     if (pt % 16 != 0) return 0;
     const int parts = cascade_parts(group_size, max_context_len, pt);
-    // partition states, then each group's partition count (groups <= sequences)
-    return (size_t)num_seqs * num_q_heads * (size_t)(parts > 0 ? parts : 1) * (2 + (size_t)head_dim) * sizeof(float) +
+    // the decode counter header (left alone), partition states, then each
+    // group's partition count (groups <= sequences)
+    return kCounterBytes +
+           (size_t)num_seqs * num_q_heads * (size_t)(parts > 0 ? parts : 1) * (2 + (size_t)head_dim) * sizeof(float) +
            (size_t)num_seqs * sizeof(int);
 }
 
@@ -579,8 +626,8 @@ int paged_decode_attention_shared_prefix(void *out, const void *q, const void *k
     p.part_blocks = pt / 16;
     p.max_parts = parts > 0 ? parts : 1;
     p.pre_parts = 0;
-    p.ws_ml = static_cast<float *>(workspace);
-    p.ws_o = static_cast<float *>(workspace) + (size_t)num_seqs * num_q_heads * p.max_parts * 2;
+    p.ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
+    p.ws_o = p.ws_ml + (size_t)num_seqs * num_q_heads * p.max_parts * 2;
     p.counters = reinterpret_cast<int *>(p.ws_o + (size_t)num_seqs * num_q_heads * p.max_parts * head_dim);
     p.group_members = group_members;
     p.shared_blocks = shared_blocks;
@@ -645,9 +692,15 @@ int paged_prefill_attention(void *out, const void *q, const void *k_cache, const
     pp.num_queries = num_queries;
     alignas(64) CUtensorMap tmk, tmv;
     int rc;
+#if PKV_PREFILL_PAIR_FASTEST
+    // pair index fastest: a (sequence, kv head)'s pairs run side by side and
+    // share its K/V in L2; the kernel issues sequences longest-first
+    const dim3 grid(pairs, num_kv_heads, num_seqs);
+#else
     // pair index slowest: CTAs start in linear order, so every sequence's
     // last (longest) pair starts before any shorter one
     const dim3 grid(num_kv_heads, num_seqs, pairs);
+#endif
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     alignas(64) CUtensorMap tmq;
     if ((rc = encode_q_map(&tmq, q, num_queries, num_q_heads, head_dim, g, tile_tokens)) != PKV_OK) return rc;
@@ -721,7 +774,9 @@ int decode_dispatch(void *out, const void *q, const void *k_cache, const void *v
     if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
         max_context_len < 0 || partition_tokens < PKV_PARTITION_BALANCED)
         return PKV_ERR_ARG;
-    if (!dtype_ok(dtype)) return PKV_ERR_UNSUPPORTED;
+    if (!dtype_ok(input_dtype(dtype))) return PKV_ERR_UNSUPPORTED;
+    const bool f32_out = dtype == PKV_BF16_OUT_F32;
+    dtype = input_dtype(dtype);
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (num_q_heads % num_kv_heads != 0) return PKV_ERR_ARG;
     const int g = num_q_heads / num_kv_heads;
@@ -764,41 +819,33 @@ int decode_dispatch(void *out, const void *q, const void *k_cache, const void *v
 
     if (persistent) {
         p.counters = static_cast<int *>(workspace);
-        p.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                               align256((size_t)num_seqs * num_kv_heads * sizeof(int)));
+        p.partials = reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes);
         alignas(64) CUtensorMap tmk, tmv;
         int rc;
         if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
         if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
-        // groups wider than 8 need two MMA column tiles: half the warps, twice the stages,
-        // so their registers fit without spilling
         constexpr int ns128 = PKV_PERSIST_STAGES_D128, ns64 = PKV_PERSIST_STAGES_D64, nw = kPersistWarps;
-        if (head_dim == 128)
-            return g <= 8 ? launch_persistent<128, 1, ns128, nw>(tmk, tmv, p, st, pdl)
-                          : launch_persistent<128, 2, 2 * ns128, nw / 2>(tmk, tmv, p, st, pdl);
-        return g <= 8 ? launch_persistent<64, 1, ns64, nw>(tmk, tmv, p, st, pdl)
-                      : launch_persistent<64, 2, 2 * ns64, nw / 2>(tmk, tmv, p, st, pdl);
+        return f32_out ? persistent_by_shape<float, ns128, ns64, nw>(tmk, tmv, p, st, pdl, head_dim, g)
+                       : persistent_by_shape<__nv_bfloat16, ns128, ns64, nw>(tmk, tmv, p, st, pdl, head_dim, g);
     }
 
     const size_t grid_ws = grid_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, pt);
-    p.ws_ml = grid_ws ? static_cast<float *>(workspace) : nullptr;
-    p.ws_o = grid_ws ? static_cast<float *>(workspace) + (size_t)num_seqs * num_q_heads * mp * 2 : nullptr;
+    p.ws_ml = grid_ws ? reinterpret_cast<float *>(static_cast<char *>(workspace) + kCounterBytes) : nullptr;
+    p.ws_o = grid_ws ? p.ws_ml + (size_t)num_seqs * num_q_heads * mp * 2 : nullptr;
     dim3 grid(mp, num_kv_heads, num_seqs);
     int rc;
     if (dtype == PKV_BF16) {
         alignas(64) CUtensorMap tmk, tmv;
         if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
         if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim)) != PKV_OK) return rc;
-        if (head_dim == 128)
-            rc = g <= 8 ? launch_bf16<128, 1>(tmk, tmv, p, grid, st, pdl)
-                        : launch_bf16<128, 2>(tmk, tmv, p, grid, st, pdl);
-        else
-            rc = g <= 8 ? launch_bf16<64, 1>(tmk, tmv, p, grid, st, pdl) : launch_bf16<64, 2>(tmk, tmv, p, grid, st, pdl);
+        rc = f32_out ? grid_by_shape<float>(tmk, tmv, p, grid, st, pdl, head_dim, g)
+                     : grid_by_shape<__nv_bfloat16>(tmk, tmv, p, grid, st, pdl, head_dim, g);
     } else {
         rc = head_dim == 128 ? launch_f32<128>(p, grid, st, pdl) : launch_f32<64>(p, grid, st, pdl);
     }
     if (rc != PKV_OK) return rc;
-    if (mp > 1) rc = head_dim == 128 ? launch_reduce<128>(p, dtype, st) : launch_reduce<64>(p, dtype, st);
+    const pkv_dtype out_dt = f32_out ? PKV_F32 : dtype;
+    if (mp > 1) rc = head_dim == 128 ? launch_reduce<128>(p, out_dt, st) : launch_reduce<64>(p, out_dt, st);
     return rc;
 }
 
@@ -872,22 +919,23 @@ extern "C" int paged_decode_step(void *out, const void *q, void *k_cache, void *
                                  const int64_t *slot_mapping, int num_tokens, const int64_t *src_dst_pairs,
                                  int num_pairs, void *stream) {
     int rc;
+    const pkv_dtype cache_dt = input_dtype(dtype);  // what append and copy move
     // every argument is checked before anything is launched
     if ((rc = decode_dispatch(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads, num_seqs,
                               num_q_heads, head_dim, max_blocks_per_seq, num_blocks, max_context_len, dtype,
                               partition_tokens, workspace, workspace_bytes, stream, kCheckOnly)) != PKV_OK)
         return rc;
     if ((rc = append_impl(k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens, num_kv_heads, head_dim, num_blocks,
-                          dtype, stream, true)) != PKV_OK)
+                          cache_dt, stream, true)) != PKV_OK)
         return rc;
     if ((rc = move_impl(k_cache, v_cache, num_blocks, k_cache, v_cache, num_blocks, src_dst_pairs, num_pairs,
-                        num_kv_heads, head_dim, dtype, stream, true)) != PKV_OK)
+                        num_kv_heads, head_dim, cache_dt, stream, true)) != PKV_OK)
         return rc;
     if ((rc = move_impl(k_cache, v_cache, num_blocks, k_cache, v_cache, num_blocks, src_dst_pairs, num_pairs,
-                        num_kv_heads, head_dim, dtype, stream, false)) != PKV_OK)
+                        num_kv_heads, head_dim, cache_dt, stream, false)) != PKV_OK)
         return rc;
     if ((rc = append_impl(k_new, v_new, slot_mapping, k_cache, v_cache, num_tokens, num_kv_heads, head_dim, num_blocks,
-                          dtype, stream, false)) != PKV_OK)
+                          cache_dt, stream, false)) != PKV_OK)
         return rc;
     return decode_dispatch(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads, num_seqs,
                            num_q_heads, head_dim, max_blocks_per_seq, num_blocks, max_context_len, dtype,

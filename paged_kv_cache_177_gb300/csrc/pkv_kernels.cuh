@@ -41,6 +41,15 @@ __device__ unsigned int g_dev_error = 0;
 
 __device__ __forceinline__ void raise_error(unsigned int bits) { atomicOr(&g_dev_error, bits); }
 
+// Output element from the fp32 result: bf16 rounded to nearest even, or the
+// fp32 value itself (bf16 inputs with fp32 output: the accumulator before
+// rounding, for error analysis).
+template <typename OutT>
+__device__ __forceinline__ OutT to_out(float v) {
+    if constexpr (sizeof(OutT) == 2) return __float2bfloat16_rn(v);
+    else return v;
+}
+
 struct DecodeParams {
     void *out;                    // [S][Hq][D]
     const void *q;                // [S][Hq][D]
@@ -55,7 +64,8 @@ struct DecodeParams {
     int max_blocks_per_seq, num_blocks, max_context_len;
     int part_blocks;              // blocks per split-context partition
     int max_parts;                // partitions allotted per (sequence, head) in the workspace
-    int *counters;                // persistent kernel: [S][Hkv] arrival counters, zero between calls;
+    int *counters;                // persistent kernel: one arrival counter per worker (indexed by the
+                                  // first worker of a cut unit), zero between calls;
                                   // shared-prefix kernel: [groups] partitions of each group's union
     float *partials;              // persistent kernel: [workers][2][g][2 + D] segment states
     // shared-prefix (cascade) decode
@@ -113,9 +123,60 @@ struct WarpAttn {
     static constexpr int kSteps = D / 16;
     static constexpr int kSubBytes = kBlock * 128;      // 2 KiB: 16 rows of 64 bf16
     static constexpr int kSub = D / 64;
+    using QFrag = uint32_t[kSteps][NT][2];
+    using Scores = float[NT][4];
     float m[NT][2], l[NT][2];
     float acc[kSteps][NT][4];
-    uint32_t qf[kSteps][NT][2];                          // Q^T as the MMA B operand
+    QFrag qf;                                            // Q^T as the MMA B operand
+
+    __device__ __forceinline__ void set_q(const QFrag &f) {
+#pragma unroll
+        for (int kk = 0; kk < kSteps; ++kk)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                qf[kk][nt][0] = f[kk][nt][0];
+                qf[kk][nt][1] = f[kk][nt][1];
+            }
+    }
+
+    // Writes the g heads' outputs O / l (after reduce_l); out_rows = [g][D].
+    template <typename OutT>
+    __device__ __forceinline__ void store_rows(OutT *out_rows, int g, int lane) const {
+        const int gq = lane >> 2, t4 = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int head = nt * 8 + 2 * t4 + (e & 1);
+                if (head < g) {
+                    const float inv = 1.f / l[nt][e & 1];
+#pragma unroll
+                    for (int mt = 0; mt < kSteps; ++mt)
+                        out_rows[(size_t)head * D + 16 * mt + gq + (e >> 1) * 8] = to_out<OutT>(acc[mt][nt][e] * inv);
+                }
+            }
+    }
+
+    // Writes the g heads' (max, sum, unnormalised acc) states (after
+    // reduce_l); slot = [g][2 + D].
+    __device__ __forceinline__ void store_state(float *slot, int g, int lane) const {
+        const int gq = lane >> 2, t4 = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int head = nt * 8 + 2 * t4 + (e & 1);
+                if (head < g) {
+                    float *row = slot + (size_t)head * (2 + D);
+                    if (gq == 0 && e < 2) {
+                        row[0] = m[nt][e];
+                        row[1] = l[nt][e];
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < kSteps; ++mt) row[2 + 16 * mt + gq + (e >> 1) * 8] = acc[mt][nt][e];
+                }
+            }
+    }
 
     __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -301,6 +362,188 @@ struct WarpAttn {
 };
 
 // =====================================================================================
+// The per-block step for one query head per kv head (MHA, g = 1) on the CUDA
+// cores. With a single query head the block's contraction is a matrix-vector
+// product -- [16 tokens x D] . q and then [D x 16] . p -- that fills one of
+// the tensor cores' eight MMA columns, so the warp does it in fp32 FMAs: the
+// staged bf16 K and V are widened exactly to fp32 and the softmax weights stay
+// fp32 (no rounding of p before P V). Same staged tiles, interface and state
+// layout as WarpAttn, so the decode kernels take either.
+//   scores: lane (quarter h4 = lane / 8, t8 = lane % 8) dots D/4 elements of
+//     tokens t8 and t8 + 8 with the matching quarter of q; the four quarters
+//     of a token are summed with two shuffles. Eight consecutive lanes read
+//     eight different rows at one logical chunk, which the 128-byte swizzle
+//     spreads over all banks.
+//   softmax: m is kept equal in every lane; each lane of quarter 0 keeps the
+//     running sum of its two tokens' weights (summed over lanes by reduce_l).
+//   P V: lane owns output elements (D/32) lane .. + D/32 - 1; token t's
+//     weight is broadcast from lane t % 8, its V row read 4 or 8 bytes a lane.
+// =====================================================================================
+template <int D>
+struct WarpAttnScalar {
+    static constexpr int kSubBytes = kBlock * 128;      // 2 KiB: 16 rows of 64 bf16
+    static constexpr int kQuarter = D / 4;              // elements of a row one lane dots
+    static constexpr int kChunks = kQuarter / 8;        // its 16-byte chunks (4 or 2)
+    static constexpr int kWords = kQuarter / 2;         // its bf16 pairs (16 or 8)
+    static constexpr int kDims = D / 32;                // output elements per lane (4 or 2)
+    using QFrag = uint32_t[kWords];                     // the lane's quarter of q, bf16 pairs
+    using Scores = float[2];                            // tokens t8 and t8 + 8
+    float m, l;
+    uint64_t acc[kDims / 2];                            // packed fp32 pairs: elements kDims*lane ..
+    QFrag qw;                                           // widened to fp32 where used
+
+    static __device__ __forceinline__ void load_q_frags(QFrag &f, const __nv_bfloat16 *q_group, int, int lane) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(q_group + (lane >> 3) * kQuarter);
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+            const uint4 v = __ldg(src + j);
+            f[4 * j + 0] = v.x;
+            f[4 * j + 1] = v.y;
+            f[4 * j + 2] = v.z;
+            f[4 * j + 3] = v.w;
+        }
+    }
+
+    __device__ __forceinline__ void set_q(const QFrag &f) {
+#pragma unroll
+        for (int i = 0; i < kWords; ++i) qw[i] = f[i];
+    }
+
+    __device__ __forceinline__ void load_q(const __nv_bfloat16 *q_group, int g, int lane) {
+        load_q_frags(qw, q_group, g, lane);
+    }
+
+    __device__ __forceinline__ void reset() {
+        m = -INFINITY;
+        l = 0.f;
+#pragma unroll
+        for (int i = 0; i < kDims / 2; ++i) acc[i] = 0;   // +0.0f, +0.0f
+    }
+
+    // s[p] = <q, K_t> for token t = t8 + 8 p of the staged K tile; each q pair
+    // is widened once for both tokens.
+    __device__ __forceinline__ void scores(uint32_t sk, Scores &s, int lane) const {
+        const int h4 = lane >> 3, t8 = lane & 7;
+        uint64_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;        // token t8: a, token t8 + 8: b
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+            const int ci = h4 * kChunks + j;             // 16-byte chunk of the D-element row
+            const int u = ci >> 3, c = ci & 7;           // 64-element sub-tile, chunk within its row
+            const uint32_t at = sk + u * kSubBytes + ((c ^ t8) << 4);   // rows t8 and t8 + 8 share the swizzle
+            uint32_t x[4], y[4];
+            ld_shared_v4(at + t8 * 128, x);
+            ld_shared_v4(at + (t8 + 8) * 128, y);
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+                const uint64_t q0 = bf16x2_to_f2(qw[4 * j + e]), q1 = bf16x2_to_f2(qw[4 * j + e + 1]);
+                a0 = fma_f2(bf16x2_to_f2(x[e]), q0, a0);
+                a1 = fma_f2(bf16x2_to_f2(x[e + 1]), q1, a1);
+                b0 = fma_f2(bf16x2_to_f2(y[e]), q0, b0);
+                b1 = fma_f2(bf16x2_to_f2(y[e + 1]), q1, b1);
+            }
+        }
+        float x0, x1, y0, y1;
+        unpack_f2(add_f2(a0, a1), x0, x1);
+        unpack_f2(add_f2(b0, b1), y0, y1);
+        float d0 = x0 + x1, d1 = y0 + y1;
+        d0 += __shfl_xor_sync(0xffffffffu, d0, 8);
+        d1 += __shfl_xor_sync(0xffffffffu, d1, 8);
+        d0 += __shfl_xor_sync(0xffffffffu, d0, 16);
+        d1 += __shfl_xor_sync(0xffffffffu, d1, 16);
+        s[0] = d0;
+        s[1] = d1;
+    }
+
+    // Online-softmax update with the block's scores, then acc += V^T p.
+    // Rows below `lo` are not tokens of the sequence (zero-filled by TMA).
+    __device__ __forceinline__ void softmax_pv(const Scores &s, uint32_t sv, int lo, float scale_log2, int lane,
+                                               int = 0, int = 0, bool = false) {
+        const int h4 = lane >> 3, t8 = lane & 7;
+        const float x0 = t8 >= lo ? s[0] * scale_log2 : -INFINITY;
+        const float x1 = t8 + 8 >= lo ? s[1] * scale_log2 : -INFINITY;
+        float mx = fmaxf(x0, x1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        const float mn = fmaxf(m, mx);                   // finite: a block holds at least one token
+        const float al = ex2_approx(m - mn);             // 0 on the first block (m = -inf)
+        const float p0 = ex2_approx(x0 - mn), p1 = ex2_approx(x1 - mn);
+        m = mn;
+        l = l * al + (h4 == 0 ? p0 + p1 : 0.f);
+        const uint64_t al2 = pack_f2(al, al);
+        uint64_t a2[kDims / 2];                          // odd tokens in a second chain
+#pragma unroll
+        for (int i = 0; i < kDims / 2; ++i) {
+            acc[i] = fma_f2(acc[i], al2, 0);
+            a2[i] = 0;
+        }
+        // this lane's elements: 16-byte chunk ci of the row, at byte `off` in it
+        constexpr int kLaneBytes = kDims * 2;
+        const int ci = (lane * kLaneBytes) >> 4, off = (lane * kLaneBytes) & 15;
+        const uint32_t vbase = sv + (ci >> 3) * kSubBytes + off;
+        const int c = ci & 7;
+        // two tokens per pass, even ones into acc and odd ones into a2; four
+        // passes unrolled at a time keep the loads in flight without spilling
+#pragma unroll 4
+        for (int t = 0; t < kBlock; t += 2) {
+            const float pe = __shfl_sync(0xffffffffu, t < 8 ? p0 : p1, t & 7);
+            const float po = __shfl_sync(0xffffffffu, t < 8 ? p0 : p1, (t + 1) & 7);
+            const uint64_t pe2 = pack_f2(pe, pe), po2 = pack_f2(po, po);
+            const uint32_t ae = vbase + t * 128 + ((c ^ (t & 7)) << 4);
+            const uint32_t ao = vbase + (t + 1) * 128 + ((c ^ ((t + 1) & 7)) << 4);
+            if constexpr (kDims == 4) {
+                uint32_t we[2], wo[2];
+                ld_shared_v2(ae, we);
+                ld_shared_v2(ao, wo);
+                acc[0] = fma_f2(bf16x2_to_f2(we[0]), pe2, acc[0]);
+                acc[1] = fma_f2(bf16x2_to_f2(we[1]), pe2, acc[1]);
+                a2[0] = fma_f2(bf16x2_to_f2(wo[0]), po2, a2[0]);
+                a2[1] = fma_f2(bf16x2_to_f2(wo[1]), po2, a2[1]);
+            } else {
+                uint32_t we, wo;
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(we) : "r"(ae));
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wo) : "r"(ao));
+                acc[0] = fma_f2(bf16x2_to_f2(we), pe2, acc[0]);
+                a2[0] = fma_f2(bf16x2_to_f2(wo), po2, a2[0]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kDims / 2; ++i) acc[i] = add_f2(acc[i], a2[i]);
+    }
+
+    __device__ __forceinline__ void reduce_l() {
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    }
+
+    template <typename OutT>
+    __device__ __forceinline__ void store_rows(OutT *out_rows, int, int lane) const {
+        const float inv = 1.f / l;
+#pragma unroll
+        for (int i = 0; i < kDims / 2; ++i) {
+            float a, b;
+            unpack_f2(acc[i], a, b);
+            out_rows[kDims * lane + 2 * i] = to_out<OutT>(a * inv);
+            out_rows[kDims * lane + 2 * i + 1] = to_out<OutT>(b * inv);
+        }
+    }
+
+    __device__ __forceinline__ void store_state(float *slot, int, int lane) const {
+        if (lane == 0) {
+            slot[0] = m;
+            slot[1] = l;
+        }
+#pragma unroll
+        for (int i = 0; i < kDims / 2; ++i) {
+            float a, b;
+            unpack_f2(acc[i], a, b);
+            slot[2 + kDims * lane + 2 * i] = a;
+            slot[2 + kDims * lane + 2 * i + 1] = b;
+        }
+    }
+};
+
+// =====================================================================================
 // K1 (bf16, grid): one CTA per (split-context partition, kv head, sequence).
 //
 // Warp NCW is the producer: it reads the partition's block ids from the table
@@ -440,7 +683,7 @@ __device__ __forceinline__ void grid_consume(WarpAttn<D, NT> &wa, int nb, BlockA
     }
 }
 
-template <int D, int NT, int NSTAGE, int NCW>
+template <int D, int NT, int NSTAGE, int NCW, typename OutT = __nv_bfloat16>
 __global__ void __launch_bounds__((NCW + 1) * 32)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const DecodeParams p) {
@@ -453,12 +696,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
     const int len = seq_len(p, s, tid == 0 && part == 0 && h == 0);
     const int nblk = (len + kBlock - 1) / kBlock;
     const int npart = (nblk + p.part_blocks - 1) / p.part_blocks;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+    OutT *out = static_cast<OutT *>(p.out);
 
     if (len == 0) {  // empty context: zero output rows
         if (part == 0) {
-            __nv_bfloat16 *o = out + ((size_t)s * p.num_q_heads + (size_t)h * g) * D;
-            for (int i = tid; i < g * D; i += C::kThreads) o[i] = __float2bfloat16_rn(0.f);
+            OutT *o = out + ((size_t)s * p.num_q_heads + (size_t)h * g) * D;
+            for (int i = tid; i < g * D; i += C::kThreads) o[i] = to_out<OutT>(0.f);
         }
         return;
     }
@@ -499,7 +742,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
         },
         p.scale_log2, base, full, empty, g, warp, lane, tid, [&](int col, int d, float o, float M, float L) {
             if (npart == 1) {
-                out[(orow0 + col) * D + d] = __float2bfloat16_rn(o);
+                out[(orow0 + col) * D + d] = to_out<OutT>(o);
             } else {
                 const size_t r = (orow0 + col) * p.max_parts + part;
                 p.ws_o[r * D + d] = o;
@@ -524,7 +767,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
 // state per unit segment. A unit that lies inside one range is written out
 // directly. A unit cut by range boundaries leaves one (max, sum, acc) state
 // per segment in the workspace; the warp that finishes the unit's last
-// outstanding segment (an arrival counter per unit) merges the segments with
+// outstanding segment (an arrival counter per cut unit, kept at the head of
+// the workspace, where no other decode path writes) merges the segments with
 // the log-sum-exp rule in segment order and writes the output, so the result
 // does not depend on which warp arrives last.
 // =====================================================================================
@@ -569,9 +813,9 @@ __device__ __forceinline__ void cursor_advance(Cursor &c, int k, const int *pref
 // writes the g output rows. One warp; lane k holds segment k's weights, and
 // every lane accumulates head-dim elements lane, lane+32, .. of all heads
 // with the loads of two segments in flight at a time.
-template <int D>
+template <int D, typename OutT>
 __device__ __forceinline__ void merge_segments(const float *partials, size_t slot_floats, int w1, int nseg, int g,
-                                               __nv_bfloat16 *out_rows, int lane) {
+                                               OutT *out_rows, int lane) {
     constexpr int PER = D / 32;
     auto seg_row = [&](int k, int head) -> const float * {
         return partials + (size_t)(2 * (w1 + k) + (k == 0 ? 1 : 0)) * slot_floats + (size_t)head * (2 + D);
@@ -629,11 +873,13 @@ __device__ __forceinline__ void merge_segments(const float *partials, size_t slo
             }
         }
 #pragma unroll
-        for (int i = 0; i < PER; ++i) out_rows[(size_t)head * D + lane + 32 * i] = __float2bfloat16_rn(acc[i]);
+        for (int i = 0; i < PER; ++i) out_rows[(size_t)head * D + lane + 32 * i] = to_out<OutT>(acc[i]);
     }
 }
 
-template <int D, int NT, int NS, int NW>
+// WA: the per-block step -- WarpAttn (tensor cores, any group up to 8 NT) or
+// WarpAttnScalar (CUDA cores, one query head per kv head).
+template <int D, int NT, int NS, int NW, typename OutT = __nv_bfloat16, class WA = WarpAttn<D, NT>>
 __global__ void __launch_bounds__(NW * 32, 1)
     decode_bf16_persistent_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                                   const DecodeParams p) {
@@ -646,7 +892,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(base + C::kBarOffset);
     int *prefix = reinterpret_cast<int *>(base + C::kPrefixOffset);
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(p.out);
+    OutT *out = static_cast<OutT *>(p.out);
 
     if (tid == 0) {
         prefetch_tensormap(&tmk);
@@ -684,8 +930,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
     // ---- empty contexts: zero output rows (spread over the CTAs) ----
     for (int s = blockIdx.x; s < S; s += gridDim.x) {
         if (prefix[s + 1] == prefix[s]) {
-            __nv_bfloat16 *o = out + (size_t)s * p.num_q_heads * D;
-            for (int i = tid; i < p.num_q_heads * D; i += C::kThreads) o[i] = __float2bfloat16_rn(0.f);
+            OutT *o = out + (size_t)s * p.num_q_heads * D;
+            for (int i = tid; i < p.num_q_heads * D; i += C::kThreads) o[i] = to_out<OutT>(0.f);
         }
     }
 
@@ -784,16 +1030,15 @@ __global__ void __launch_bounds__(NW * 32, 1)
         issue_v();
     }
 
-    const int gq = lane >> 2, t4 = lane & 3;
     const size_t slot_floats = (size_t)g * (2 + D);
-    WarpAttn<D, NT> wa;
+    WA wa;
     int seg_j0 = c.j;
     int len = seq_len(p, c.s, false);
     wa.load_q(static_cast<const __nv_bfloat16 *>(p.q) + ((size_t)c.s * p.num_q_heads + (size_t)c.h * g) * D, g, lane);
     wa.reset();
 
     const __nv_bfloat16 *qbase = static_cast<const __nv_bfloat16 *>(p.q);
-    uint32_t qnext[C::kSteps][NT][2];
+    typename WA::QFrag qnext;
     int len_next = 0;
     for (int i = 0; i < cnt; ++i) {
         const int st = i % NS;
@@ -802,8 +1047,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
         if (unit_end && i != cnt - 1) {
             // the next unit's query and length, in flight while this block computes
             cursor_advance(cn, 1, prefix, Hkv);
-            WarpAttn<D, NT>::load_q_frags(qnext, qbase + ((size_t)cn.s * p.num_q_heads + (size_t)cn.h * g) * D, g,
-                                          lane);
+            WA::load_q_frags(qnext, qbase + ((size_t)cn.s * p.num_q_heads + (size_t)cn.h * g) * D, g, lane);
             len_next = seq_len(p, cn.s, false);
         }
         const uint32_t sk = smem_u32(ring + st * C::kStage);
@@ -812,7 +1056,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
             raise_error(PKV_DEVERR_TIMEOUT);
             break;
         }
-        float sc[NT][4];
+        typename WA::Scores sc;
         wa.scores(sk, sc, lane);
         __syncwarp();  // every lane's K fragment loads are done before the K refill
         const bool refill = kissued < cnt;
@@ -834,50 +1078,26 @@ __global__ void __launch_bounds__(NW * 32, 1)
         wa.reduce_l();
         const size_t orow0 = (size_t)c.s * p.num_q_heads + (size_t)c.h * g;
         if (seg_j0 == 0 && unit_end) {
-            // the whole unit: write the output from the fragments
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int head = nt * 8 + 2 * t4 + (e & 1);
-                    if (head < g) {
-                        const float inv = 1.f / wa.l[nt][e & 1];
-#pragma unroll
-                        for (int mt = 0; mt < C::kSteps; ++mt)
-                            out[(orow0 + head) * D + 16 * mt + gq + (e >> 1) * 8] =
-                                __float2bfloat16_rn(wa.acc[mt][nt][e] * inv);
-                    }
-                }
+            // the whole unit: write the output from the registers
+            wa.store_rows(out + orow0 * D, g, lane);
         } else {
             // a cut unit: leave this segment's state, then the last arrival merges
-            float *mine = p.partials + (size_t)(2 * w + (seg_j0 == 0 ? 1 : 0)) * slot_floats;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int head = nt * 8 + 2 * t4 + (e & 1);
-                    if (head < g) {
-                        float *row = mine + (size_t)head * (2 + D);
-                        if (gq == 0 && e < 2) {
-                            row[0] = wa.m[nt][e];
-                            row[1] = wa.l[nt][e];
-                        }
-#pragma unroll
-                        for (int mt = 0; mt < C::kSteps; ++mt) row[2 + 16 * mt + gq + (e >> 1) * 8] = wa.acc[mt][nt][e];
-                    }
-                }
+            wa.store_state(p.partials + (size_t)(2 * w + (seg_j0 == 0 ? 1 : 0)) * slot_floats, g, lane);
             __syncwarp();  // every lane's state writes are ordered before lane 0's release below
-            const int u = c.s * Hkv + c.h;
-            int prev = 0;
-            if (lane == 0) prev = atomic_add_acq_rel_gpu(p.counters + u, 1);
-            prev = __shfl_sync(0xffffffffu, prev, 0);
+            // workers w1..w2 cover the unit; w1 (the worker holding its first
+            // position) is the first worker of no other cut unit -- only one
+            // unit spans the end of a worker's range -- so counters[w1] is
+            // this unit's own arrival counter
             const long long x0 = (long long)Hkv * prefix[c.s] + (long long)c.h * c.n;
             const int w1 = (int)(((x0 + 1) * W - 1) / T);
             const int w2 = (int)(((x0 + c.n) * W - 1) / T);
+            int prev = 0;
+            if (lane == 0) prev = atomic_add_acq_rel_gpu(p.counters + w1, 1);
+            prev = __shfl_sync(0xffffffffu, prev, 0);
             if (prev == w2 - w1) {
                 __syncwarp();  // lane 0's acquire covers the lanes reading the other segments
-                merge_segments<D>(p.partials, slot_floats, w1, w2 - w1 + 1, g, out + orow0 * D, lane);
-                if (lane == 0) p.counters[u] = 0;  // ready for the next call
+                merge_segments<D, OutT>(p.partials, slot_floats, w1, w2 - w1 + 1, g, out + orow0 * D, lane);
+                if (lane == 0) p.counters[w1] = 0;  // ready for the next call
             }
         }
         if (i == cnt - 1) break;
@@ -885,13 +1105,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
         c = cn;
         seg_j0 = 0;
         len = len_next;
-#pragma unroll
-        for (int kk = 0; kk < C::kSteps; ++kk)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                wa.qf[kk][nt][0] = qnext[kk][nt][0];
-                wa.qf[kk][nt][1] = qnext[kk][nt][1];
-            }
+        wa.set_q(qnext);
         wa.reset();
     }
 }

@@ -99,6 +99,37 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+#ifndef PKV_PREFILL_PAIR_FASTEST
+#define PKV_PREFILL_PAIR_FASTEST 0
+#endif
+constexpr int kRankMaxSeqs = 128;  // batches up to this size are issued longest-first
+
+// The sequence a CTA with sequence rank z works on: in batches of up to
+// kRankMaxSeqs sequences, the z-th by new-token count (most first, ties by
+// index); larger batches in index order. Warp 0 ranks the counts from
+// shared memory; every thread of the CTA calls it (it holds a barrier).
+__device__ __forceinline__ int prefill_sequence_by_rank(const PrefillParams &pp, int z, int tid) {
+    const int S = pp.d.num_seqs;
+    if (S > kRankMaxSeqs) return z;
+    __shared__ int counts[kRankMaxSeqs];
+    __shared__ int chosen;
+    if (tid < 32) {
+        for (int i = tid; i < S; i += 32) counts[i] = __ldg(pp.query_start + i + 1) - __ldg(pp.query_start + i);
+        __syncwarp();
+        for (int i = tid; i < S; i += 32) {
+            const int ni = counts[i];
+            int rank = 0;
+            for (int j = 0; j < S; ++j) {
+                const int nj = counts[j];
+                rank += (nj > ni || (nj == ni && j < i)) ? 1 : 0;
+            }
+            if (rank == z) chosen = i;
+        }
+    }
+    __syncthreads();
+    return chosen;
+}
+
 template <int D>
 __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -106,15 +137,26 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
     using C = TcCfg<D>;
     const DecodeParams &p = pp.d;
     extern __shared__ uint8_t smem_raw[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+#if PKV_PREFILL_PAIR_FASTEST
+    // grid (pairs, kv heads, sequence rank): the pairs of one (sequence, kv
+    // head) run side by side and read its K/V while it sits in L2; the
+    // longest (last) pair of each starts first, and so does the sequence with
+    // the most new tokens
+    const int pair = gridDim.x - 1 - blockIdx.x, h = blockIdx.y;
+    const int s = prefill_sequence_by_rank(pp, blockIdx.z, tid);
+    const bool flagger = blockIdx.x == 0 && h == 0;
+#else
     const int h = blockIdx.x, s = blockIdx.y;
     const int pair = gridDim.z - 1 - blockIdx.z;  // the longest (last) tiles start first
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool flagger = blockIdx.z == 0 && h == 0;
+#endif
     const int g = p.group;
     const int q0 = __ldg(pp.query_start + s), n = __ldg(pp.query_start + s + 1) - q0;
-    const int len = seq_len(p, s, tid == 0 && blockIdx.z == 0 && h == 0);
+    const int len = seq_len(p, s, tid == 0 && flagger);
     const int tt = pp.tile_tokens;
     if (n < 0 || n > len || n > pp.max_query_len || q0 < 0 || q0 + n > pp.num_queries) {
-        if (tid == 0 && blockIdx.z == 0 && h == 0) raise_error(PKV_DEVERR_LENGTH);
+        if (tid == 0 && flagger) raise_error(PKV_DEVERR_LENGTH);
         return;
     }
     if (pair * C::kTiles * tt >= n) return;

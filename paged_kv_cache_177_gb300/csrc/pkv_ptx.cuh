@@ -322,6 +322,22 @@ __device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
     return d;
 }
 
+// 16- and 8-byte shared-memory loads.
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ld_shared_v2(uint32_t addr, uint32_t (&r)[2]) {
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
+
+// The two bf16 of a 32-bit word as a packed fp32 pair (element at the lower
+// address first): widening bf16 is exact, the bits move to the top half.
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
+    return pack_f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 // 16-byte shared-memory store.
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)

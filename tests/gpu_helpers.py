@@ -63,3 +63,36 @@ def assert_caches_equal(w, h):
         got = W.to_numpy(getattr(w, name)).view(np.uint8)
         exp = h[name].view(np.uint8)
         assert np.array_equal(got, exp), f"{name} after copy_blocks + kv_append differs from the oracle"
+
+
+EDGE_LENGTHS = (0, 1, 15, 16, 17, 31, 33, 64, 100, 255, 511, 512, 513, 1000, 1537, 7)
+
+
+def path_switching_calls():
+    """Decode calls that take the decode paths in turn, for one reused
+    workspace: (label, host workload, partition_tokens, persistent?).
+
+    1. a few long 13B-class sequences, automatic partitioning: the split grid
+       kernel, whose partial states land in the workspace;
+    2. a 13B-class batch of 64, automatic: the persistent kernel, whose
+       arrival counters must read zero although call 1 wrote partials;
+    3. fixed 128-token partitions on a GQA batch with edge lengths;
+    4. a larger GQA batch, automatic: the persistent kernel again."""
+    return [
+        ("grid split", W.make_workload("mha13b", lengths_list=(600, 1500, 2048, 513, 1024, 77, 1800, 900),
+                                       seed=301), 0, False),
+        ("persistent", W.make_workload("mha13b", seed=302), 0, True),
+        ("fixed partitions", W.make_workload("gqa8b", lengths_list=EDGE_LENGTHS, seed=303), 128, False),
+        ("persistent, larger batch", W.make_workload("gqa8b", num_seqs=160, len_hi=1500, seed=304), 0, True),
+    ]
+
+
+def prepared(case):
+    """GPU copy of a path_switching_calls case after its copies and appends,
+    and the oracle's output for it (every sequence, every head)."""
+    label, wc, pt, persistent = case
+    h = host_arrays(wc)
+    ref = oracle_step(h, wc.layout, wc.scale)
+    w = wc.to("cuda")
+    gpu_step(w, attention=False)
+    return w, ref

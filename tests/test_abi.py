@@ -59,9 +59,21 @@ def test_partition_and_workspace_sizing(binding):
     assert binding.partition_tokens(8, 8, 131072, 512) == 512
     # a context no longer than one partition needs no workspace
     assert binding.workspace_bytes(64, 40, 40, 128, 512, 512) == 0
-    # otherwise: S * Hq * ceil(L / P) * (2 + D) floats
-    assert binding.workspace_bytes(8, 64, 8, 128, 131072, 512) == 8 * 64 * 256 * 130 * 4
-    assert binding.workspace_bytes(2, 4, 4, 64, 1000, 64) == 2 * 4 * 16 * 66 * 4
+    # otherwise: the counter header, then S * Hq * ceil(L / P) * (2 + D) floats
+    hdr = binding.DECODE_COUNTER_BYTES
+    assert binding.workspace_bytes(8, 64, 8, 128, 131072, 512) == hdr + 8 * 64 * 256 * 130 * 4
+    assert binding.workspace_bytes(2, 4, 4, 64, 1000, 64) == hdr + 2 * 4 * 16 * 66 * 4
+    # the persistent layout does not depend on the batch size: one state per
+    # group head for two segments of each of up to 160 x 16 workers
+    for S in (1, 64, 8192):
+        assert binding.workspace_bytes(S, 32, 8, 128, 64, -1) == hdr + 160 * 16 * 2 * 4 * 130 * 4
+
+
+def test_counter_header_size_matches_the_header():
+    from paged_kv_cache_177_gb300 import binding as b
+    m = re.search(r"#define\s+PKV_DECODE_COUNTER_BYTES\s+(\d+)u?", open(HEADER).read())
+    assert m and int(m.group(1)) == b.DECODE_COUNTER_BYTES
+    assert b.DECODE_COUNTER_BYTES % 256 == 0 and b.DECODE_COUNTER_BYTES >= 160 * 16 * 4
 
 
 def test_which_decode_kernel_runs(binding):
@@ -108,6 +120,18 @@ def test_decode_rejects_bad_arguments_before_any_cuda_call(lib):
     assert _decode(lib, maxlen=4096, pt=64) == -6    # split needed, no workspace
     assert _decode(lib, scale=float("nan")) == -1
     assert _decode(lib, S=0) == 0                    # empty batch: nothing to do
+    # bf16 inputs with fp32 output: the same checks apply
+    assert _decode(lib, dtype=2, d=96) == -2
+    assert _decode(lib, dtype=2, maxlen=4096, pt=64) == -6
+    assert _decode(lib, dtype=2, S=0) == 0
+    assert _decode(lib, dtype=3) == -2
+
+
+def test_fp32_output_mode_plans_like_bf16(lib):
+    for fn, args in (("pkv_decode_persistent", (64, 40, -1)), ("pkv_decode_launches", (64, 40, 4096, -1))):
+        f = getattr(lib, fn)
+        f.restype = ctypes.c_int
+        assert f(*args, 2) == f(*args, 1) != f(*args, 0)
 
 
 def _prefill(lib, **kw):
@@ -125,6 +149,7 @@ def _prefill(lib, **kw):
 
 def test_prefill_rejects_bad_arguments_before_any_cuda_call(lib):
     assert _prefill(lib, dtype=0) == -2              # fp32 prefill is not provided
+    assert _prefill(lib, dtype=2) == -2              # nor fp32 output
     assert _prefill(lib, d=96) == -2
     assert _prefill(lib, hq=12, hkv=8) == -1
     assert _prefill(lib, hq=8 * 65, hkv=8) == -2     # group of 65 > the largest supported (64)

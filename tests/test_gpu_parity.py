@@ -6,8 +6,7 @@ oracle, element by element on the same seeded inputs.
   for fp32.
 Small cases span several blocks, several partitions and ragged tails; the
 full-size workloads run in the launch configuration the benchmark times and
-are checked on sampled sequences (all heads) plus size-independent
-properties on every output.
+are checked on every sequence and head.
 """
 import zlib
 
@@ -20,7 +19,7 @@ from tests import gpu_helpers as H
 
 pytestmark = pytest.mark.gpu
 
-EDGE_LENGTHS = (0, 1, 15, 16, 17, 31, 33, 64, 100, 255, 511, 512, 513, 1000, 1537, 7)
+EDGE_LENGTHS = H.EDGE_LENGTHS
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -216,49 +215,36 @@ def test_device_error_word_and_validators():
 
 # ---- full-size workloads, in the benchmark's launch configuration ----------------------
 
-FULL = {
-    # name: sampled sequences checked against the oracle (all heads)
-    "mha13b": 8,
-    "gqa8b": 8,
-    "parallel_sampling": 8,
-    "long_context": 2,
-}
+FULL = ["mha13b", "gqa8b", "parallel_sampling", "long_context"]
 
 
-@pytest.mark.parametrize("name", list(FULL))
+@pytest.mark.parametrize("name", FULL)
 def test_full_size_workload(name):
+    """The benchmarked batches, in the benchmark's launch configuration:
+    caches bit-exact after the step's copies and appends, and every output
+    element of every sequence and head within the bf16 bound of the oracle."""
     w = W.make_workload(name, device="cuda")
     lay = w.layout
     h = H.host_arrays(w)
     out = H.gpu_step(w, lay.spec.partition_tokens)
     torch.cuda.synchronize()
-    order = np.argsort(lay.context_lens, kind="stable")
-    extra = np.random.default_rng(0).choice(len(order), max(0, FULL[name] - 2), replace=False).tolist()
-    pick = sorted(set([int(order[-1]), int(order[0])] + extra))
-    ref = H.oracle_step(h, lay, w.scale, seq_ids=pick)
+    ref = H.oracle_step(h, lay, w.scale)
     H.assert_caches_equal(w, h)
-    H.assert_close(out[torch.as_tensor(pick, device="cuda")], ref, lay.spec.dtype, name)
-    # every output: finite, and a convex combination of values that are N(0,1)-sized
-    o = out.float()
-    assert torch.isfinite(o).all()
-    vmax = torch.nan_to_num(w.v_cache.float(), nan=0.0).abs().max()
-    assert float(o.abs().max()) <= float(vmax) * (1 + 1e-2)
+    H.assert_close(out, ref, lay.spec.dtype, name)
 
 
 @pytest.mark.parametrize("name", ["mha13b", "gqa8b", "long_context"])
 def test_full_size_fp32(name):
     """The 13B-class, GQA and long-context batches with fp32 caches (the
-    CUDA-core path): sampled sequences against the oracle at the fp32 bound."""
+    CUDA-core path): every sequence and head against the oracle at the fp32
+    bound."""
     w = W.make_workload(name, device="cuda", dtype="f32")
     lay = w.layout
     h = H.host_arrays(w)
     out = H.gpu_step(w, lay.spec.partition_tokens)
     torch.cuda.synchronize()
-    order = np.argsort(lay.context_lens, kind="stable")
-    pick = sorted({int(order[-1]), int(order[0]), int(order[len(order) // 2])})
-    ref = H.oracle_step(h, lay, w.scale, seq_ids=pick)
-    H.assert_close(out[torch.as_tensor(pick, device="cuda")], ref, "f32", f"{name} fp32")
-    assert torch.isfinite(out).all()
+    ref = H.oracle_step(h, lay, w.scale)
+    H.assert_close(out, ref, "f32", f"{name} fp32")
 
 
 def test_persistent_path_leaves_counters_zero_and_repeats_bit_identically():
@@ -282,12 +268,39 @@ def test_persistent_path_leaves_counters_zero_and_repeats_bit_identically():
             b.paged_decode_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
                                      max_context_len=lay.max_context_len, workspace=ws, partition_tokens=-1)
             torch.cuda.synchronize()
-            counters = ws[: lay.spec.num_seqs * hkv * 4]
+            counters = ws[: b.DECODE_COUNTER_BYTES]
             assert int(counters.count_nonzero()) == 0
             outs.append(out)
         assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
         ref = H.oracle_step(h, lay, w.scale)
         H.assert_close(outs[0], ref, "bf16", f"persistent {lens}")
+
+
+def test_one_workspace_serves_every_decode_path_in_turn():
+    """One workspace, zero-filled once and sized for the largest call, serves
+    a split grid call, a persistent call, a fixed-partition call and a
+    persistent call on a larger batch, in that order (a serving loop whose
+    batch crosses the persistent threshold): every output matches the oracle
+    on every sequence and head, and the counter header is zero after each
+    call."""
+    b = H.lib()
+    cases = H.path_switching_calls()
+    need = max(b.workspace_bytes(wc.spec.num_seqs, wc.spec.num_q_heads, wc.spec.num_kv_heads, wc.spec.head_dim,
+                                 wc.layout.max_context_len, pt) for _, wc, pt, _ in cases)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    for case in cases + cases[:2]:
+        label, wc, pt, persistent = case
+        sp, lay = wc.spec, wc.layout
+        assert b.decode_persistent(sp.num_seqs, sp.num_kv_heads, pt, torch.bfloat16) == persistent, label
+        assert persistent or b.decode_launches(sp.num_seqs, sp.num_kv_heads, lay.max_context_len, pt) == 2, label
+        w, ref = H.prepared(case)
+        out = torch.full_like(w.q, float("nan"))
+        b.paged_decode_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
+                                 max_context_len=lay.max_context_len, partition_tokens=pt, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(ws[: b.DECODE_COUNTER_BYTES].count_nonzero()) == 0, label
+        H.assert_close(out, ref, "bf16", f"reused workspace, {label}")
+        del w
 
 
 LARGE_CASES = [
@@ -303,7 +316,7 @@ def test_persistent_large_batches(case):
     """Batches of at least 8 positions per persistent warp: every warp's
     range cuts units at both ends, so nearly every warp writes segment
     states and many merge; the arrival counters are zero after each call, the
-    output repeats bit for bit and matches the oracle on sampled sequences."""
+    output repeats bit for bit and matches the oracle on every sequence."""
     name, hq, hkv, S, longest = case
     b = H.lib()
     rng = np.random.default_rng(zlib.crc32(name.encode()))
@@ -322,17 +335,11 @@ def test_persistent_large_batches(case):
         b.paged_decode_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
                                  max_context_len=lay.max_context_len, workspace=ws, partition_tokens=-1)
         torch.cuda.synchronize()
-        assert int(ws[: S * hkv * 4].count_nonzero()) == 0
+        assert int(ws[: b.DECODE_COUNTER_BYTES].count_nonzero()) == 0
         outs.append(out)
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
-    order = np.argsort(np.asarray(lens), kind="stable")
-    pick = sorted(set([int(order[0]), int(order[-1])] + rng.choice(S, 10, replace=False).tolist()))
-    ref = H.oracle_step(h, lay, w.scale, seq_ids=pick)
-    H.assert_close(outs[0][torch.as_tensor(pick, device="cuda")], ref, "bf16", name)
-    o = outs[0].float()
-    assert torch.isfinite(o).all()
-    vmax = torch.nan_to_num(w.v_cache.float(), nan=0.0).abs().max()   # free blocks hold NaN
-    assert float(o.abs().max()) <= float(vmax) * (1 + 1e-2)
+    ref = H.oracle_step(h, lay, w.scale)
+    H.assert_close(outs[0], ref, "bf16", name)
 
 
 def test_persistent_step_in_a_cuda_graph():

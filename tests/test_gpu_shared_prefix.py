@@ -79,15 +79,13 @@ def test_full_size_parallel_sampling_against_plain_decode():
     b.paged_decode_attention(plain, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
                              max_context_len=lay.max_context_len)
     out = _run(w, lay.group_members, lay.shared_blocks)
-    # both within the bf16 tolerance of the oracle on a sample, and of each other everywhere
+    # both within the bf16 tolerance of the oracle on every sequence and head
     h = H.host_arrays(w)
-    pick = [0, 1, 77, 127]
     import oracle
     ref = oracle.paged_decode_attention(h["q"], h["k_cache"], h["v_cache"], lay.block_tables, lay.context_lens,
-                                        w.scale, lay.spec.num_kv_heads, seq_ids=pick)
-    H.assert_close(out[torch.tensor(pick, device="cuda")], ref, "bf16", "full size shared prefix")
-    diff = (out.float() - plain.float()).abs()
-    assert float(diff.max()) < 4e-3 + 2e-2 * float(plain.float().abs().max())
+                                        w.scale, lay.spec.num_kv_heads)
+    H.assert_close(out, ref, "bf16", "full size shared prefix")
+    H.assert_close(plain, ref, "bf16", "full size plain decode of the shared-prefix batch")
 
 
 def test_one_uncleared_workspace_serves_every_partition_size():

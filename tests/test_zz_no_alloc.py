@@ -4,18 +4,17 @@ Some callers cannot allocate device memory where they call this library -- a
 plugin or extension hook that is handed raw device pointers and has no
 allocator, or a serving loop that owns all device memory from start-up and
 forbids later cudaMalloc.  For them the split-context scratch lives in the
-library's own device array.  These tests call that entry point through the C
-ABI and check it against paged_decode_attention (which takes a caller
-workspace) on the same inputs, for two calls in a row with different shapes,
-so the second call runs over whatever the first left in the shared array.
+library's own device array, shared by every call.  These tests call that
+entry point through the C ABI, calls in a row that take the split grid and
+the persistent paths in turn (each call runs over whatever the one before
+left in the array), and check every output against the oracle and against
+paged_decode_attention with a fresh zero-filled workspace of its own.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
-from paged_kv_cache_177_gb300 import workloads as W
 from tests import gpu_helpers as H
 
 pytestmark = pytest.mark.gpu
@@ -41,36 +40,56 @@ def _call_static(fn, out, w, partition_tokens):
               partition_tokens, torch.cuda.current_stream().cuda_stream)
 
 
-def _reference(w, partition_tokens):
+def _with_own_workspace(w, partition_tokens):
     b = H.lib()
-    out = torch.empty_like(w.q)
+    out = torch.full_like(w.q, float("nan"))
     b.paged_decode_attention(out, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale,
                              max_context_len=w.layout.max_context_len, partition_tokens=partition_tokens)
     return out
 
 
-def test_static_workspace_matches_the_workspace_entry_point_on_two_calls_in_a_row():
+def _run(fn, case):
+    label, wc, pt, persistent = case
+    b = H.lib()
+    sp = wc.spec
+    need = b.workspace_bytes(sp.num_seqs, sp.num_q_heads, sp.num_kv_heads, sp.head_dim, wc.layout.max_context_len, pt)
+    assert 0 < need <= STATIC_BYTES, label           # the call really uses the scratch
+    assert b.decode_persistent(sp.num_seqs, sp.num_kv_heads, pt, torch.bfloat16) == persistent, label
+    w, ref = H.prepared(case)
+    out = torch.full_like(w.q, float("nan"))
+    assert _call_static(fn, out, w, pt) == 0, label
+    own = _with_own_workspace(w, pt)
+    torch.cuda.synchronize()
+    H.assert_close(out, ref, sp.dtype, f"static workspace, {label}")
+    H.assert_close(out, own.double().cpu().numpy(), sp.dtype, f"static vs own workspace, {label}")
+
+
+def test_static_workspace_matches_the_oracle_on_calls_that_switch_paths():
+    """Split grid, persistent, fixed partitions, persistent on a larger batch,
+    then split grid and persistent again -- six calls in a row on the one
+    array."""
     torch.cuda.set_device(0)
     fn = _entry()
-    b = H.lib()
+    cases = H.path_switching_calls()
+    for case in cases + cases[:2]:
+        _run(fn, case)
+    assert H.lib().device_error(clear=True) == 0
+
+
+def test_static_workspace_two_calls_in_a_row_balanced_request():
+    """The balanced split asked for explicitly (PKV_PARTITION_BALANCED) on two
+    different batches, one after the other."""
+    torch.cuda.set_device(0)
+    fn = _entry()
+    from paged_kv_cache_177_gb300 import workloads as W
     cases = [
-        (W.make_workload("gqa8b", lengths_list=(1, 17, 700, 2000, 0, 1537, 64, 999), seed=11), 64),
-        (W.make_workload("mha13b", lengths_list=(300, 1, 33, 1200, 515), num_q_heads=6, num_kv_heads=6,
-                         head_dim=64, seed=12), 48),
+        ("balanced, GQA edge lengths", W.make_workload("gqa8b", lengths_list=H.EDGE_LENGTHS, seed=11), -1, True),
+        ("balanced, MHA d=64", W.make_workload("mha13b", lengths_list=(300, 1, 33, 1200, 515), num_q_heads=6,
+                                               num_kv_heads=6, head_dim=64, seed=12), -1, True),
     ]
-    for wc, pt in cases:
-        w = wc.to("cuda")
-        H.gpu_step(w, attention=False)
-        sp = w.spec
-        need = b.workspace_bytes(sp.num_seqs, sp.num_q_heads, sp.num_kv_heads, sp.head_dim,
-                                 w.layout.max_context_len, pt)
-        assert 0 < need <= STATIC_BYTES          # the call really uses the scratch
-        ref = _reference(w, pt)
-        out = torch.full_like(w.q, float("nan"))
-        assert _call_static(fn, out, w, pt) == 0
-        torch.cuda.synchronize()
-        H.assert_close(out, ref.double().cpu().numpy(), sp.dtype, f"static workspace, {sp.name}")
-    assert b.device_error(clear=True) == 0
+    for case in cases:
+        _run(fn, case)
+    assert H.lib().device_error(clear=True) == 0
 
 
 def test_static_workspace_rejects_requests_beyond_its_size():
