@@ -33,6 +33,7 @@ import argparse
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -81,28 +82,105 @@ def peaks():
 
 
 # Committed ncu summaries that hold a kernel's DRAM traffic per launch on a
-# workload, valid while the kernel sources still hash to the recorded value.
+# workload, valid while the source the kernel is built and launched from is
+# unchanged: a sha256 over the definitions each kernel depends on (its own
+# code, the device helpers and per-block steps it calls, the host code that
+# encodes its tensor maps and launches it), comments and whitespace removed.
+# A change anywhere else in the same files leaves the capture valid.
 PROFILED = {
     ("mha13b", "decode_bf16_persistent_kernel"): "decode_bf16_persistent_kernel_mha13b.md",
     ("gqa8b", "decode_bf16_persistent_kernel"): "decode_bf16_persistent_kernel_gqa8b.md",
     ("long_context", "decode_bf16_kernel"): "decode_bf16_kernel_long_context.md",
 }
-KERNEL_SOURCES = ["include/pagedkv.h", "paged_kv_cache_177_gb300/csrc/pkv.cu",
-                  "paged_kv_cache_177_gb300/csrc/pkv_kernels.cuh", "paged_kv_cache_177_gb300/csrc/pkv_ptx.cuh"]
+_CSRC = "paged_kv_cache_177_gb300/csrc/"
+_DEVICE_COMMON = ["kBlock", "kSplitBlocks", "g_dev_error", "raise_error", "to_out", "DecodeParams", "seq_len",
+                  "WarpAttn"]
+_HOST_COMMON = ["PKV_GRID_STAGES", "PKV_GRID_CONSUMERS", "PKV_PERSIST_WARPS", "PKV_PERSIST_STAGES_D128",
+                "PKV_PERSIST_STAGES_D64", "PKV_PERSIST_MAX_SEQS", "PKV_MHA_CUDA_CORES", "kCounterBytes", "kPersistWarps", "kPersistMaxCtas", "kPersistMaxSeqs", "kNstage", "kNcw",
+                "kSmemLimit", "launch_pdl", "encode_fn", "encode_cache_map", "max_parts_for", "sm_count",
+                "decode_dispatch", "pkv_decode_partition_tokens", "pkv_decode_workspace_bytes",
+                "grid_workspace_bytes", "persist_workspace_bytes", "input_dtype", "use_persistent"]
+KERNEL_SPANS = {
+    "decode_bf16_persistent_kernel": {
+        "include/pagedkv.h": None, _CSRC + "pkv_ptx.cuh": None,
+        _CSRC + "pkv_kernels.cuh": _DEVICE_COMMON + ["WarpAttnScalar", "PersistCfg", "Cursor", "cursor_advance",
+                                                     "merge_segments", "decode_bf16_persistent_kernel"],
+        _CSRC + "pkv.cu": _HOST_COMMON + ["kMhaCudaCores", "launch_persistent", "persistent_by_shape"],
+    },
+    "decode_bf16_kernel": {
+        "include/pagedkv.h": None, _CSRC + "pkv_ptx.cuh": None,
+        _CSRC + "pkv_kernels.cuh": _DEVICE_COMMON + ["Bf16Cfg", "grid_produce", "grid_consume",
+                                                     "decode_bf16_kernel", "block_reduce", "lse_reduce_kernel"],
+        _CSRC + "pkv.cu": _HOST_COMMON + ["launch_bf16", "grid_by_shape", "launch_reduce"],
+    },
+}
 
 
-def kernel_sources_sha256() -> str:
-    """sha256 of the kernel sources with comments and whitespace removed, so
-    that only a change to the code itself invalidates a capture."""
+def _strip_comments(text: str) -> str:
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    return re.sub(r"//[^\n]*", " ", text)
+
+
+def _matching(text: str, i: int, open_c: str, close_c: str) -> int:
+    """Index just past the bracket that closes the one at text[i]."""
+    depth = 0
+    for j in range(i, len(text)):
+        if text[j] == open_c:
+            depth += 1
+        elif text[j] == close_c:
+            depth -= 1
+            if depth == 0:
+                return j + 1
+    raise ValueError("unbalanced source")
+
+
+def definition_spans(text: str, name: str):
+    """The definitions of ``name`` in C++ source ``text`` (comments removed):
+    a struct or class body, a function body, a constant or variable up to its
+    semicolon, or a #define line. Calls and declarations are not definitions."""
+    spans = []
+    for m in re.finditer(r"\b%s\b" % re.escape(name), text):
+        i, j = m.start(), m.end()
+        line_start = text.rfind("\n", 0, i) + 1
+        before = text[line_start:i]
+        if before.strip() == "#define":
+            spans.append(text[line_start:text.find("\n", j)])
+            continue
+        if re.search(r"\b(struct|class)\s*$", before):
+            brace, semi = text.find("{", j), text.find(";", j)
+            if brace != -1 and (semi == -1 or brace < semi):
+                spans.append(text[i:_matching(text, brace, "{", "}")])
+            continue
+        k = j
+        while k < len(text) and text[k].isspace():
+            k += 1
+        if k < len(text) and text[k] == "(":
+            close = _matching(text, k, "(", ")")
+            rest = re.match(r"\s*(const\s*)?\{", text[close:])
+            if rest and not re.search(r"[=(,]\s*$", before):
+                brace = close + rest.end() - 1
+                spans.append(text[i:_matching(text, brace, "{", "}")])
+            continue
+        if k < len(text) and text[k] in "=[" and re.search(r"\b(constexpr|__device__|const)\b", before):
+            spans.append(text[line_start:text.find(";", j) + 1])
+    return spans
+
+
+def kernel_source_sha256(kernel: str) -> str:
+    """sha256 of the source spans ``kernel`` is built and launched from."""
     import hashlib
-    import re
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f, names in KERNEL_SPANS[kernel].items():
         with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
-            text = fh.read()
-        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-        text = re.sub(r"//[^\n]*", " ", text)
-        h.update(" ".join(text.split()).encode())
+            text = _strip_comments(fh.read())
+        parts = [text] if names is None else []
+        for n in names or ():
+            found = definition_spans(text, n)
+            if not found:
+                raise KeyError(f"{n} has no definition in {f}")
+            parts.extend(found)
+        for part in parts:
+            h.update(" ".join(part.split()).encode())
     return h.hexdigest()
 
 
@@ -118,7 +196,7 @@ def profiled_traffic(workload: str, kernel: str):
                           if line.startswith(("traffic_bytes_per_launch: ", "source_sha256: ")))
     except OSError:
         return None, f"profiles/{name} missing"
-    if fields.get("source_sha256", "").strip() != kernel_sources_sha256():
+    if fields.get("source_sha256", "").strip() != kernel_source_sha256(kernel):
         return None, f"kernel sources changed since profiles/{name} was captured"
     return int(fields["traffic_bytes_per_launch"]), f"profiles/{name}"
 
@@ -473,7 +551,8 @@ def run_ours(args, rank, world, local, dist):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    sp = W.spec(args.workload, seed=W.spec(args.workload).seed + 7919 * rank)
+    over = {"dtype": args.dtype} if args.dtype else {}
+    sp = W.spec(args.workload, seed=W.spec(args.workload).seed + 7919 * rank, **over)
     pt = args.partition_tokens if args.partition_tokens is not None else sp.partition_tokens
     w = W.make_workload(sp, device=dev)
     lay = w.layout
@@ -660,9 +739,11 @@ def run_ours(args, rank, world, local, dist):
             (parity is None or parity["within_bound"]) and
             all(c["parity"]["within_bound"] for c in configs.values() if isinstance(c, dict)))
     srt = sorted(step_ms)
-    roof_kernel = "decode_bf16_persistent_kernel" if persistent else "decode_bf16_kernel"
+    roof_kernel = ("decode_bf16_persistent_kernel" if persistent else
+                   "decode_bf16_kernel" if sp.dtype == "bf16" else "decode_f32_kernel")
     # the captures were taken on the workloads' default launch configuration
-    traffic, traffic_src = profiled_traffic(sp.name if args.partition_tokens is None else "", roof_kernel)
+    traffic, traffic_src = profiled_traffic(sp.name if args.partition_tokens is None and args.dtype is None else "",
+                                            roof_kernel)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -693,8 +774,8 @@ def run_ours(args, rank, world, local, dist):
         "pct_hbm_peak": {"measured": round(100 * value / world / peak, 2),
                          "nominal_7.9TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2)},
         "roofline": {
-            "kernel": "paged_decode_attention (" + ("decode_bf16_persistent_kernel" if persistent else
-                                                    "decode_bf16_kernel" + (" + lse_reduce_kernel" if attn_launches == 2 else "")) + ")",
+            "kernel": "paged_decode_attention (" + (roof_kernel if persistent else
+                                                    roof_kernel + (" + lse_reduce_kernel" if attn_launches == 2 else "")) + ")",
             "bound": "hbm", "achieved": round(attn_gbs, 2), "peak": peak, "unit": "GB/s",
             "frac": round(attn_gbs / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
             "traffic": traffic, "traffic_source": traffic_src,
@@ -979,6 +1060,8 @@ def main():
                     help="oracle seconds per extra configuration's cpu_baseline")
     ap.add_argument("--no-configs", action="store_true", help="time the headline workload only")
     ap.add_argument("--partition-tokens", type=int, default=None)
+    ap.add_argument("--dtype", choices=["bf16", "f32"], default=None,
+                    help="cache dtype (default: the workload's own); f32 runs the CUDA-core fp32 path")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -990,7 +1073,8 @@ def main():
         ap.error("at least 3 warm-up steps")
     if args.impl == "reference" and args.steps is None:
         args.steps = 5
-    args.all_configs = args.workload is None and not args.no_configs and args.partition_tokens is None
+    args.all_configs = (args.workload is None and not args.no_configs and args.partition_tokens is None
+                        and args.dtype is None)
     if args.workload is None:
         args.workload = "mha13b"
     rank, world, local, dist = dist_setup(args)

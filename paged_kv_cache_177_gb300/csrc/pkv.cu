@@ -149,11 +149,11 @@ int max_parts_for(int max_context_len, int part_tokens) {
     return (max_context_len + part_tokens - 1) / part_tokens;
 }
 
-template <int D, int NT, typename OutT>
+template <int D, int NT, typename OutT, class WA = pkv::WarpAttn<D, NT>>
 int launch_bf16(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, dim3 grid,
                 cudaStream_t st, bool pdl = false) {
     using C = pkv::Bf16Cfg<D, NT, kNstage, kNcw>;
-    auto kern = pkv::decode_bf16_kernel<D, NT, kNstage, kNcw, OutT>;
+    auto kern = pkv::decode_bf16_kernel<D, NT, kNstage, kNcw, OutT, WA>;
     static thread_local int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -298,9 +298,9 @@ int launch_persistent(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv:
 // Head-dim and group-width dispatch of the two bf16 decode kernels: groups
 // wider than 8 need two MMA column tiles (the persistent kernel then runs
 // half the warps with twice the stages, so their registers fit unspilled).
-// One query head per kv head (g = 1) takes the CUDA-core step: the block's
-// contraction is then a matrix-vector product that would fill one of the
-// tensor cores' eight MMA columns.
+// One query head per kv head (g = 1) takes the CUDA-core step in both
+// kernels: the block's contraction is then a matrix-vector product that
+// would fill one of the tensor cores' eight MMA columns.
 template <typename OutT, int NS128, int NS64, int NW>
 int persistent_by_shape(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, cudaStream_t st,
                         bool pdl, int head_dim, int g) {
@@ -319,9 +319,14 @@ int persistent_by_shape(const CUtensorMap &tmk, const CUtensorMap &tmv, const pk
 template <typename OutT>
 int grid_by_shape(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, dim3 grid,
                   cudaStream_t st, bool pdl, int head_dim, int g) {
-    if (head_dim == 128)
+    if (head_dim == 128) {
+        if (g == 1 && kMhaCudaCores)
+            return launch_bf16<128, 1, OutT, pkv::WarpAttnScalar<128>>(tmk, tmv, p, grid, st, pdl);
         return g <= 8 ? launch_bf16<128, 1, OutT>(tmk, tmv, p, grid, st, pdl)
                       : launch_bf16<128, 2, OutT>(tmk, tmv, p, grid, st, pdl);
+    }
+    if (g == 1 && kMhaCudaCores)
+        return launch_bf16<64, 1, OutT, pkv::WarpAttnScalar<64>>(tmk, tmv, p, grid, st, pdl);
     return g <= 8 ? launch_bf16<64, 1, OutT>(tmk, tmv, p, grid, st, pdl)
                   : launch_bf16<64, 2, OutT>(tmk, tmv, p, grid, st, pdl);
 }
@@ -692,15 +697,14 @@ int paged_prefill_attention(void *out, const void *q, const void *k_cache, const
     pp.num_queries = num_queries;
     alignas(64) CUtensorMap tmk, tmv;
     int rc;
-#if PKV_PREFILL_PAIR_FASTEST
-    // pair index fastest: a (sequence, kv head)'s pairs run side by side and
-    // share its K/V in L2; the kernel issues sequences longest-first
-    const dim3 grid(pairs, num_kv_heads, num_seqs);
-#else
-    // pair index slowest: CTAs start in linear order, so every sequence's
-    // last (longest) pair starts before any shorter one
-    const dim3 grid(num_kv_heads, num_seqs, pairs);
-#endif
+    // CTA order. Whole prompts (context not much longer than the new tokens):
+    // the pair index slowest, so every sequence's last (longest) pair starts
+    // before any shorter one. Chunks after a cached context at least as long
+    // as the chunk: one sequence at a time (longest first), so the pairs of a
+    // (sequence, kv head) read its K/V from L2 -- there each pair attends the
+    // whole cached context, and re-reading it from DRAM dominates.
+    pp.seq_major = max_context_len >= 2 * max_query_len ? 1 : 0;
+    const dim3 grid = pp.seq_major ? dim3(num_kv_heads, pairs, num_seqs) : dim3(num_kv_heads, num_seqs, pairs);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     alignas(64) CUtensorMap tmq;
     if ((rc = encode_q_map(&tmq, q, num_queries, num_q_heads, head_dim, g, tile_tokens)) != PKV_OK) return rc;

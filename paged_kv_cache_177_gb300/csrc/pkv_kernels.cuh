@@ -157,6 +157,32 @@ struct WarpAttn {
             }
     }
 
+    // Writes every column's (max, sum) into ml [8 NT][2] and unnormalised
+    // acc into the rows of acc_rows [8 NT][stride] (after reduce_l), for a
+    // merge of several warps' states.
+    __device__ __forceinline__ void store_merge(float *ml, float *acc_rows, int stride, int lane) const {
+        const int gq = lane >> 2, t4 = lane & 3;
+        if (gq == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int head = nt * 8 + 2 * t4 + c;
+                    ml[head * 2 + 0] = m[nt][c];
+                    ml[head * 2 + 1] = l[nt][c];
+                }
+        }
+#pragma unroll
+        for (int mt = 0; mt < kSteps; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int head = nt * 8 + 2 * t4 + (e & 1);
+                    acc_rows[head * stride + 16 * mt + gq + (e >> 1) * 8] = acc[mt][nt][e];
+                }
+    }
+
     // Writes the g heads' (max, sum, unnormalised acc) states (after
     // reduce_l); slot = [g][2 + D].
     __device__ __forceinline__ void store_state(float *slot, int g, int lane) const {
@@ -528,6 +554,27 @@ struct WarpAttnScalar {
         }
     }
 
+    __device__ __forceinline__ void block(uint32_t sk, uint32_t sv, int lo, float scale_log2, int lane, int = 0,
+                                          int = 0, bool = false) {
+        Scores sc;
+        scores(sk, sc, lane);
+        softmax_pv(sc, sv, lo, scale_log2, lane);
+    }
+
+    __device__ __forceinline__ void store_merge(float *ml, float *acc_rows, int, int lane) const {
+        if (lane == 0) {
+            ml[0] = m;
+            ml[1] = l;
+        }
+#pragma unroll
+        for (int i = 0; i < kDims / 2; ++i) {
+            float a, b;
+            unpack_f2(acc[i], a, b);
+            acc_rows[kDims * lane + 2 * i] = a;
+            acc_rows[kDims * lane + 2 * i + 1] = b;
+        }
+    }
+
     __device__ __forceinline__ void store_state(float *slot, int, int lane) const {
         if (lane == 0) {
             slot[0] = m;
@@ -624,11 +671,10 @@ __device__ __forceinline__ void grid_produce(const CUtensorMap &tmk, const CUten
 // each column c < ncols (an MMA column: a query head of a query sequence)
 // and head-dim index d, emit(c, d, o, M, L) receives the column's output
 // o = O / L and its (max, sum) in the log2 domain.
-template <class C, int D, int NT, int NSTAGE, int NCW, class BlockArgs, class Emit>
-__device__ __forceinline__ void grid_consume(WarpAttn<D, NT> &wa, int nb, BlockArgs block_args, float scale_log2,
-                                             uint8_t *base, uint64_t *full, uint64_t *empty, int ncols, int warp,
-                                             int lane, int tid, Emit emit) {
-    const int gq = lane >> 2, t4 = lane & 3;
+template <class C, int D, int NSTAGE, int NCW, class WA, class BlockArgs, class Emit>
+__device__ __forceinline__ void grid_consume(WA &wa, int nb, BlockArgs block_args, float scale_log2, uint8_t *base,
+                                             uint64_t *full, uint64_t *empty, int ncols, int warp, int lane, int tid,
+                                             Emit emit) {
     for (int j = warp; j < nb; j += NCW) {
         const int st = j % NSTAGE;
         if (!mbar_wait(&full[st], (j / NSTAGE) & 1)) {
@@ -645,26 +691,7 @@ __device__ __forceinline__ void grid_consume(WarpAttn<D, NT> &wa, int nb, BlockA
     named_barrier_sync(1, NCW * 32);  // every consumer is done with the stage ring
     float *mml = reinterpret_cast<float *>(base);                    // [NCW][kHeads][2]
     float *macc = mml + NCW * C::kHeads * 2;                         // [NCW][kHeads][kMergeStride]
-    if (gq == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int head = nt * 8 + 2 * t4 + c;
-                mml[(warp * C::kHeads + head) * 2 + 0] = wa.m[nt][c];
-                mml[(warp * C::kHeads + head) * 2 + 1] = wa.l[nt][c];
-            }
-    }
-#pragma unroll
-    for (int mt = 0; mt < C::kSteps; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int head = nt * 8 + 2 * t4 + (e & 1);
-                const int d = 16 * mt + gq + (e >> 1) * 8;
-                macc[(warp * C::kHeads + head) * C::kMergeStride + d] = wa.acc[mt][nt][e];
-            }
+    wa.store_merge(mml + warp * C::kHeads * 2, macc + warp * C::kHeads * C::kMergeStride, C::kMergeStride, lane);
     named_barrier_sync(1, NCW * 32);
     for (int idx = tid; idx < ncols * D; idx += NCW * 32) {
         const int col = idx / D, d = idx - col * D;
@@ -683,7 +710,7 @@ __device__ __forceinline__ void grid_consume(WarpAttn<D, NT> &wa, int nb, BlockA
     }
 }
 
-template <int D, int NT, int NSTAGE, int NCW, typename OutT = __nv_bfloat16>
+template <int D, int NT, int NSTAGE, int NCW, typename OutT = __nv_bfloat16, class WA = WarpAttn<D, NT>>
 __global__ void __launch_bounds__((NCW + 1) * 32)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const DecodeParams p) {
@@ -730,12 +757,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
                                 last_valid, p.num_blocks, p.num_kv_heads, h, base, full, empty, lane);
         return;
     }
-    WarpAttn<D, NT> wa;
+    WA wa;
     wa.load_q(static_cast<const __nv_bfloat16 *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)h * g) * D, g, lane);
     wa.reset();
     const size_t orow0 = (size_t)s * p.num_q_heads + (size_t)h * g;
     const int last_in_range = (b_begin + nb - 1 == nblk - 1) ? nb - 1 : -1;
-    grid_consume<C, D, NT, NSTAGE, NCW>(
+    grid_consume<C, D, NSTAGE, NCW>(
         wa, nb,
         [&](int j, int) {
             return make_int4(j == last_in_range ? kBlock - last_valid : 0, 0, C::kHeads, b_begin + j < kSplitBlocks);
@@ -1269,7 +1296,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32)
     wa.load_q_rows(static_cast<const __nv_bfloat16 *>(p.q), row_of, lane);
     wa.reset();
     const int ncols = min(u.count * g, C::kHeads);
-    grid_consume<C, D, NT, NSTAGE, NCW>(
+    grid_consume<C, D, NSTAGE, NCW>(
         wa, nb,
         [&](int, int st) {
             const int2 info = stage_info[st];
@@ -1372,6 +1399,7 @@ struct PrefillParams {
     int tile_tokens;             // query tokens per 128-row tile (128 / g)
     int max_query_len;           // the grid covers this many new tokens per sequence
     int num_queries;             // rows of q and out
+    int seq_major;               // CTA order: one sequence at a time (1) or pair index slowest (0)
 };
 
 // =====================================================================================

@@ -99,10 +99,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-#ifndef PKV_PREFILL_PAIR_FASTEST
-#define PKV_PREFILL_PAIR_FASTEST 0
-#endif
-constexpr int kRankMaxSeqs = 128;  // batches up to this size are issued longest-first
+constexpr int kRankMaxSeqs = 128;  // batches up to this size can be issued longest-first
 
 // The sequence a CTA with sequence rank z works on: in batches of up to
 // kRankMaxSeqs sequences, the z-th by new-token count (most first, ties by
@@ -138,19 +135,23 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
     const DecodeParams &p = pp.d;
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-#if PKV_PREFILL_PAIR_FASTEST
-    // grid (pairs, kv heads, sequence rank): the pairs of one (sequence, kv
-    // head) run side by side and read its K/V while it sits in L2; the
-    // longest (last) pair of each starts first, and so does the sequence with
-    // the most new tokens
-    const int pair = gridDim.x - 1 - blockIdx.x, h = blockIdx.y;
-    const int s = prefill_sequence_by_rank(pp, blockIdx.z, tid);
-    const bool flagger = blockIdx.x == 0 && h == 0;
-#else
-    const int h = blockIdx.x, s = blockIdx.y;
-    const int pair = gridDim.z - 1 - blockIdx.z;  // the longest (last) tiles start first
-    const bool flagger = blockIdx.z == 0 && h == 0;
-#endif
+    // Two CTA orders (the grid's shape follows pp.seq_major):
+    //  - grid (kv heads, sequences, pairs), the pair index slowest and taken from the
+    //    last: every sequence's longest pairs start first and the short ones fill the end;
+    //  - grid (kv heads, pairs, sequence rank): one sequence at a time, sequences in
+    //    decreasing order of new tokens, each one's longest pairs first over its kv heads;
+    //    a (sequence, kv head)'s pairs start num_kv_heads CTAs apart, so they read its
+    //    K/V while it is in L2 without streaming it in lockstep.
+    const int h = blockIdx.x;
+    int s, pair;
+    if (pp.seq_major) {
+        pair = gridDim.y - 1 - blockIdx.y;
+        s = prefill_sequence_by_rank(pp, blockIdx.z, tid);
+    } else {
+        s = blockIdx.y;
+        pair = gridDim.z - 1 - blockIdx.z;
+    }
+    const bool flagger = h == 0 && pair == 0;  // one CTA per sequence reports a bad length
     const int g = p.group;
     const int q0 = __ldg(pp.query_start + s), n = __ldg(pp.query_start + s + 1) - q0;
     const int len = seq_len(p, s, tid == 0 && flagger);

@@ -1,11 +1,14 @@
 """bench.py reports a kernel's DRAM traffic from a committed ncu summary only
-while the kernel sources are the ones the summary was captured from."""
+while the source spans the kernel is built and launched from are the ones
+the summary was captured from."""
+import pytest
+
 import bench
 
 
 def test_traffic_comes_from_the_matching_summary():
     t, src = bench.profiled_traffic("mha13b", "decode_bf16_persistent_kernel")
-    if t is None:                           # the kernel sources changed since the capture
+    if t is None:                           # the kernel's sources changed since the capture
         assert "changed since profiles/decode_bf16_persistent_kernel_mha13b.md" in src
     else:
         assert src == "profiles/decode_bf16_persistent_kernel_mha13b.md" and t > 600_000_000
@@ -14,13 +17,13 @@ def test_traffic_comes_from_the_matching_summary():
 def test_traffic_follows_the_recorded_fingerprint(monkeypatch):
     with open(bench.os.path.join(bench.ROOT, "profiles", "decode_bf16_persistent_kernel_mha13b.md")) as f:
         sha = [ln.split(": ", 1)[1].strip() for ln in f if ln.startswith("source_sha256: ")][0]
-    monkeypatch.setattr(bench, "kernel_sources_sha256", lambda: sha)
+    monkeypatch.setattr(bench, "kernel_source_sha256", lambda kernel: sha)
     t, src = bench.profiled_traffic("mha13b", "decode_bf16_persistent_kernel")
     assert src == "profiles/decode_bf16_persistent_kernel_mha13b.md" and t > 600_000_000
 
 
 def test_traffic_is_null_once_the_sources_change(monkeypatch):
-    monkeypatch.setattr(bench, "kernel_sources_sha256", lambda: "0" * 64)
+    monkeypatch.setattr(bench, "kernel_source_sha256", lambda kernel: "0" * 64)
     t, why = bench.profiled_traffic("mha13b", "decode_bf16_persistent_kernel")
     assert t is None and "changed" in why
 
@@ -28,3 +31,45 @@ def test_traffic_is_null_once_the_sources_change(monkeypatch):
 def test_traffic_is_null_without_a_capture():
     t, why = bench.profiled_traffic("parallel_sampling", "decode_bf16_persistent_kernel")
     assert t is None and "no ncu capture" in why
+
+
+@pytest.mark.parametrize("kernel", sorted(bench.KERNEL_SPANS))
+def test_every_fingerprinted_definition_exists(kernel):
+    assert len(bench.kernel_source_sha256(kernel)) == 64
+
+
+def test_definition_spans_find_definitions_not_uses():
+    src = """
+    #define N_MAX 8
+    constexpr int kBlock = 16;
+    struct Thing { int a; int f() { return 1; } };
+    __device__ int helper(int x) { if (x) { return 2; } return kBlock; }
+    void user() { helper(3); int y = helper(4); Thing t; }
+    int helper(int x);
+    """
+    assert [s.split()[0] for s in bench.definition_spans(src, "helper")] == ["helper(int"]
+    assert bench.definition_spans(src, "helper")[0].rstrip().endswith("return kBlock; }")
+    assert bench.definition_spans(src, "Thing")[0].endswith("return 1; } }")
+    assert bench.definition_spans(src, "kBlock") == ["    constexpr int kBlock = 16;"]
+    assert bench.definition_spans(src, "N_MAX") == ["    #define N_MAX 8"]
+
+
+def test_a_change_outside_the_spans_keeps_the_fingerprint(monkeypatch, tmp_path):
+    """Editing code the kernel does not depend on (here the prefill launch)
+    leaves its fingerprint unchanged; editing its own body changes it."""
+    import shutil
+    root = tmp_path / "r"
+    for f in {f for spans in bench.KERNEL_SPANS.values() for f in spans}:
+        (root / f).parent.mkdir(parents=True, exist_ok=True)
+        shutil.copy(bench.os.path.join(bench.ROOT, f), root / f)
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    k = "decode_bf16_persistent_kernel"
+    before = bench.kernel_source_sha256(k)
+    cu = root / bench._CSRC / "pkv.cu"
+    text = cu.read_text()
+    cu.write_text(text.replace("int paged_prefill_attention(", "int unused_marker = 1;\nint paged_prefill_attention(", 1))
+    assert bench.kernel_source_sha256(k) == before
+    kern = root / bench._CSRC / "pkv_kernels.cuh"
+    t2 = kern.read_text()
+    kern.write_text(t2.replace("if (i == cnt - 1) break;", "if (i == cnt - 1) { break; }", 1))
+    assert bench.kernel_source_sha256(k) != before

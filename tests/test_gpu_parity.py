@@ -477,3 +477,4 @@ def test_decode_step_call_matches_the_three_calls(name, pt, over):
         assert torch.equal(out.cpu().view(iv), out_ref.cpu().view(iv)), f"{name} {variant}"
         assert torch.equal(d.k_cache.view(iv), ref_d.k_cache.view(iv)) and torch.equal(d.v_cache.view(iv),
                                                                                         ref_d.v_cache.view(iv))
+

@@ -161,3 +161,32 @@ def test_long_prefix_chunks_sampled():
                                                  np.ascontiguousarray(hs["block_tables"][s:s + 1]), cut,
                                                  np.array([0, 4], np.int32), w.scale, w.spec.num_kv_heads)
             H.assert_close(out[torch.from_numpy(rows).cuda()], ref, "bf16", f"long prefix seq {s} rows {first}..")
+
+
+@pytest.mark.parametrize("num_seqs", [24, 130])
+def test_cta_order_does_not_change_the_result(num_seqs):
+    """The grid is issued pair index slowest when the contexts are not much
+    longer than the new tokens, else one sequence at a time in decreasing order
+    of new tokens (ranked inside the kernel for batches of up to 128 sequences,
+    in index order beyond). A larger host bound on the context length selects
+    the second order for the same inputs: the outputs are bit-identical, and
+    match the oracle. Lengths repeat, so the ranking meets ties."""
+    rng = np.random.default_rng(num_seqs)
+    new = tuple(int(x) for x in rng.choice([1, 7, 64, 130, 300] if num_seqs < 100 else [1, 7, 40, 150], num_seqs))
+    prior = tuple(int(x) for x in rng.choice([0, 5, 100], num_seqs))
+    w = W.make_prefill("chunked_gqa", new_list=new, prior_list=prior, seed=num_seqs)
+    h = _host(w)
+    ref = _oracle(h, w)
+    wg = w.to("cuda")
+    b = H.lib()
+    b.kv_append(wg.k_new, wg.v_new, wg.slot_mapping, wg.k_cache, wg.v_cache)
+    outs = []
+    assert w.max_context_len < 2 * w.max_query_len          # the default bound gives the first order
+    for bound in (w.max_context_len, max(w.max_context_len, 2 * w.max_query_len)):
+        out = torch.full_like(wg.q, float("nan"))
+        b.paged_prefill_attention(out, wg.q, wg.k_cache, wg.v_cache, wg.block_tables, wg.context_lens,
+                                  wg.query_start, wg.scale, max_query_len=w.max_query_len, max_context_len=bound)
+        torch.cuda.synchronize()
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    H.assert_close(outs[0], ref, "bf16", f"{num_seqs} sequences")
