@@ -478,3 +478,45 @@ def test_decode_step_call_matches_the_three_calls(name, pt, over):
         assert torch.equal(d.k_cache.view(iv), ref_d.k_cache.view(iv)) and torch.equal(d.v_cache.view(iv),
                                                                                         ref_d.v_cache.view(iv))
 
+
+@pytest.mark.parametrize("where", ["first blocks of other sequences", "last blocks"])
+def test_decode_step_with_appends_anywhere_matches_the_three_calls(where):
+    """paged_decode_step launches the attention right behind its append and
+    waits for the append before reading the caches: slots aimed at the first
+    (earliest-read) blocks of other sequences, and the usual last-block slots,
+    both give the bits of the three separate calls on the persistent path, and
+    the oracle's result."""
+    b = H.lib()
+    wc = W.make_workload("gqa8b", lengths_list=tuple(range(40, 40 + 97 * 23, 23)), seed=313)
+    lay = wc.layout
+    S = lay.spec.num_seqs
+    slots = lay.slot_mapping.copy()
+    if where.startswith("first"):
+        # the newest positions (NaN until appended) get this step's rows, as if appended earlier ...
+        for t, slot in enumerate(slots.tolist()):
+            wc.k_cache[slot // 16, :, slot % 16] = wc.k_new[t]
+            wc.v_cache[slot // 16, :, slot % 16] = wc.v_new[t]
+        # ... and token t now overwrites slot 3 of sequence t+1's first block (every sequence has 3+ blocks)
+        slots = np.array([int(lay.block_tables[(t + 1) % S][0]) * 16 + 3 for t in range(S)], np.int64)
+        assert len(set(slots.tolist())) == S
+    lay.slot_mapping[:] = slots
+    wc.slot_mapping.copy_(torch.from_numpy(slots))
+    h = H.host_arrays(wc)
+    ref = H.oracle_step(h, lay, wc.scale)
+    outs = []
+    for one_call in (False, True):
+        d = wc.to("cuda")
+        ws = torch.zeros(b.workspace_bytes(S, 32, 8, 128, lay.max_context_len, -1), dtype=torch.uint8, device="cuda")
+        out = torch.full_like(d.q, float("nan"))
+        if one_call:
+            b.paged_decode_step(out, d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, wc.scale, d.k_new,
+                                d.v_new, d.slot_mapping, None, max_context_len=lay.max_context_len,
+                                partition_tokens=-1, workspace=ws)
+        else:
+            b.kv_append(d.k_new, d.v_new, d.slot_mapping, d.k_cache, d.v_cache)
+            b.paged_decode_attention(out, d.q, d.k_cache, d.v_cache, d.block_tables, d.context_lens, wc.scale,
+                                     max_context_len=lay.max_context_len, partition_tokens=-1, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16)), where
+    H.assert_close(outs[1], ref, "bf16", where)
