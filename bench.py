@@ -23,7 +23,11 @@ Without ``--workload`` the line headlines mha13b (the 13B-class batch) and
 adds a ``configs`` object: every other configuration of the workload set
 (tiny, gqa8b, parallel_sampling, long_context) timed the same way (step and
 attention call), checked against the oracle on every sequence, and with the
-oracle's own rate on the host cores.
+oracle's own rate on the host cores; and ``next_rows``: the shared-prefix
+decode call on parallel_sampling (against plain decode, oracle on every
+sequence) and a prefill step on each prefill workload (TFLOP/s against the
+measured bf16 peak; the two shortest prompts against the oracle, every
+prompt's last row against the decode kernels).
 Under torchrun every rank runs its own replica of the workload (weak
 scaling): the path has no exchange step.
 """
@@ -727,7 +731,7 @@ def run_ours(args, rank, world, local, dist):
         out32 = unrounded_output(B, w, lay, pt, ws, stream)
         torch.cuda.synchronize(dev)
         parity = full_parity(lay, host, out, sp.dtype, out32)
-    configs = None
+    configs = next_rows = None
     if world == 1 and args.all_configs:
         # the other configurations of the workload set, each measured and
         # checked the same way (the headline's buffers are released first)
@@ -738,6 +742,10 @@ def run_ours(args, rank, world, local, dist):
         configs["all_within_bound"] = bool(
             (parity is None or parity["within_bound"]) and
             all(c["parity"]["within_bound"] for c in configs.values() if isinstance(c, dict)))
+        # the rows beyond the decode step: shared-prefix decode and prefill, each timed and checked
+        next_rows = {"shared_prefix": shared_prefix_measure(args.config_steps // 10, dev, B, evict),
+                     "prefill": {name: prefill_measure(name, 30, dev, B, evict, oracle_seqs=2)
+                                 for name in W.PREFILL_SPECS}}
     srt = sorted(step_ms)
     roof_kernel = ("decode_bf16_persistent_kernel" if persistent else
                    "decode_bf16_kernel" if sp.dtype == "bf16" else "decode_f32_kernel")
@@ -797,6 +805,7 @@ def run_ours(args, rank, world, local, dist):
         "parity": parity,
         "wall_s_timed_region": round(wall, 3),
         "configs": configs,
+        "next_rows": next_rows,
     }
     print(json.dumps(line), flush=True)
 
@@ -823,6 +832,19 @@ def run_op(args, rank, world, local, dist):
     torch.cuda.set_device(dev)
     if args.op == "prefill":
         return run_prefill(args, dev, B)
+    if args.op == "shared_prefix":
+        evict = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev).fill_(1.0)
+        res = shared_prefix_measure(args.steps or 50, dev, B, evict)
+        if not res["parity"]["within_bound"]:
+            raise RuntimeError(f"shared-prefix output outside the bound: {res['parity']}")
+        line = {"metric": "shared-prefix decode attention, logical KV GB/s", "unit": "GB/s",
+                "value": res["shared_prefix"]["logical_GBps"], "higher_is_better": True,
+                "config": {"workload": res["workload"], "groups": res["groups"],
+                           "shared_blocks": res["shared_blocks"]},
+                "op": "shared_prefix", "n_gpus": 1, "dtype": "bf16", "data": "synthetic"}
+        line.update({k: v for k, v in res.items() if k not in ("workload", "groups", "shared_blocks")})
+        print(json.dumps(line), flush=True)
+        return
     sp = W.spec(args.workload)
     w = W.make_workload(sp, device=dev)
     lay = w.layout
@@ -851,50 +873,7 @@ def run_op(args, rank, world, local, dist):
         t = sorted(a.elapsed_time(b) for a, b in evs)
         return t[len(t) // 2] / 1e3
 
-    if args.op == "shared_prefix":
-        H = sp.num_q_heads
-        groups = torch.from_numpy(lay.group_members).to(dev)
-        shared = torch.from_numpy(lay.shared_blocks).to(dev)
-        if groups.shape[0] == 0:
-            raise SystemExit("--op shared_prefix needs a workload with shared prompts (parallel_sampling)")
-        out_c, out_p = torch.empty_like(w.q), torch.empty_like(w.q)
-        maxlen = lay.max_context_len
-        ws_c = torch.empty(B.shared_prefix_workspace_bytes(sp.num_seqs, H, sp.head_dim, maxlen, groups.shape[1]),
-                           dtype=torch.uint8, device=dev)
-        ws_p = torch.zeros(max(16, B.workspace_bytes(sp.num_seqs, H, sp.num_kv_heads, sp.head_dim, maxlen)),
-                           dtype=torch.uint8, device=dev)
-        # the step's writes, in the step's order: copy-on-write copies, then the new tokens
-        B.copy_blocks(w.k_cache, w.v_cache, w.cow_pairs, host_pairs=lay.cow_pairs)
-        B.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
-        t_c = time_it(lambda: B.paged_decode_attention_shared_prefix(
-            out_c, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, groups, shared,
-            max_context_len=maxlen, workspace=ws_c), args.steps or 50)
-        t_p = time_it(lambda: B.paged_decode_attention(
-            out_p, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, max_context_len=maxlen,
-            workspace=ws_p), args.steps or 50)
-        # both calls attend the same contexts: finite outputs that agree to the bf16 tolerance
-        torch.cuda.synchronize(dev)
-        if not (bool(torch.isfinite(out_c.float()).all()) and bool(torch.isfinite(out_p.float()).all())):
-            raise RuntimeError("non-finite attention output in the shared-prefix benchmark")
-        diff = float((out_c.float() - out_p.float()).abs().max())
-        if diff > 4e-3 + 2e-2 * float(out_p.float().abs().max()):
-            raise RuntimeError(f"shared-prefix and plain decode outputs differ by {diff}")
-        if B.device_error(clear=True):
-            raise RuntimeError("device error word set during the shared-prefix benchmark")
-        logical, unique = lay.kv_bytes(eb), lay.unique_kv_bytes(eb)
-        peak, kind = peaks()
-        line = {"metric": "shared-prefix decode attention, logical KV GB/s", "unit": "GB/s",
-                "value": round(logical / t_c / 1e9, 2),
-                "shared_prefix": {"us": round(t_c * 1e6, 2), "logical_GB/s": round(logical / t_c / 1e9, 2),
-                                  "unique_GB/s": round(unique / t_c / 1e9, 2),
-                                  "unique_frac_of_peak": round(unique / t_c / 1e9 / peak, 4)},
-                "plain_decode": {"us": round(t_p * 1e6, 2), "logical_GB/s": round(logical / t_p / 1e9, 2)},
-                "speedup": round(t_p / t_c, 3), "logical_bytes": int(logical), "unique_bytes": int(unique),
-                "max_abs_diff_vs_plain_decode": diff,
-                "peak": peak, "peak_kind": kind, "higher_is_better": True,
-                "config": {"workload": describe(sp), "groups": int(groups.shape[0]),
-                           "shared_blocks": int(lay.shared_blocks[0])}}
-    elif args.op == "swap":
+    if args.op == "swap":
         seqs = np.arange(0, sp.num_seqs, 4)
         nblk = (lay.context_lens.astype(np.int64) + 15) // 16
         blocks = np.concatenate([lay.block_tables[s, :nblk[s]] for s in seqs]).astype(np.int64)
@@ -990,10 +969,16 @@ def tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def run_prefill(args, dev, B):
-    w = W.make_prefill(args.prefill_workload, device=dev)
+def prefill_measure(name: str, n: int, dev, B, evict, oracle_seqs: int = 0) -> dict:
+    """One prefill step (kv_append of every new token, then causal prefill
+    attention) on workload ``name``: both timed as CUDA graphs (median of ``n``
+    replays after an L2 eviction), each prompt's last row checked against the
+    decode kernels, and the ``oracle_seqs`` shortest prompts against the
+    oracle (every row, every head)."""
+    w = W.make_prefill(name, device=dev)
     sp = w.spec
-    evict = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev).fill_(1.0)
+    host = ({k: W.to_numpy(getattr(w, k)) for k in ("q", "k_cache", "v_cache", "k_new", "v_new")}
+            if oracle_seqs else None)
     out = torch.empty_like(w.q)
     mq, mc = w.max_query_len, w.max_context_len
 
@@ -1005,11 +990,10 @@ def run_prefill(args, dev, B):
         B.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
         attention()
 
-    n = args.steps or 30
     t_step = graph_time(step, n, dev, evict)
     t_attn = graph_time(attention, n, dev, evict)
-    # Each prompt's last query row attends its whole context: the decode kernels (mma.sync,
-    # no code shared with the tcgen05 prefill kernel) must give the same row.
+    # Each prompt's last query row attends its whole context: the decode kernels (CUDA cores or
+    # mma.sync, no code shared with the tcgen05 prefill kernel) must give the same row.
     torch.cuda.synchronize(dev)
     if not bool(torch.isfinite(out.float()).all()):
         raise RuntimeError("non-finite prefill attention output")
@@ -1029,19 +1013,102 @@ def run_prefill(args, dev, B):
     flops = w.flops()
     peak, kind = tensor_peak()
     tflops = flops / t_attn / 1e12
+    res = {"workload": f"{sp.name}: {sp.num_seqs} seqs, {sp.num_q_heads} q / {sp.num_kv_heads} kv heads, head_dim "
+                       f"{sp.head_dim}, bf16, block 16, new tokens {sp.new_lengths} [{sp.new_lo}, {sp.new_hi}], "
+                       f"prior context [{sp.prior_lo}, {sp.prior_hi}]",
+           "attention": {"us": round(t_attn * 1e6, 2), "TFLOP/s": round(tflops, 2),
+                         "frac_of_peak": round(tflops / peak, 4), "peak": peak, "peak_kind": kind},
+           "step": {"us": round(t_step * 1e6, 2), "tokens_per_s": round(T / t_step, 1),
+                    "what": "kv_append of every new token + prefill attention"},
+           "flops": int(flops), "new_tokens": T,
+           "check": {"last_rows_vs_decode_max_abs_diff": diff, "rows": int(len(has))}}
+    if oracle_seqs:
+        import oracle
+        hs = w.host
+        oracle.kv_append(host["k_new"], host["v_new"], hs["slot_mapping"], host["k_cache"], host["v_cache"])
+        nq = np.diff(hs["query_start"])
+        seqs = [int(i) for i in np.argsort(nq, kind="stable") if nq[i] > 0][:oracle_seqs]
+        rows = np.concatenate([np.arange(hs["query_start"][i], hs["query_start"][i + 1]) for i in seqs])
+        sub_qs = np.concatenate([[0], np.cumsum([nq[i] for i in seqs])]).astype(np.int32)
+        ref = oracle.paged_prefill_attention(np.ascontiguousarray(host["q"][rows]), host["k_cache"],
+                                             host["v_cache"], np.ascontiguousarray(hs["block_tables"][seqs]),
+                                             np.ascontiguousarray(hs["context_lens"][seqs]), sub_qs, w.scale,
+                                             sp.num_kv_heads, nthreads=cpu_cores())
+        got = out[torch.from_numpy(rows).to(dev)].float().cpu().numpy().astype(np.float64)
+        err = np.abs(got - ref)
+        res["parity"] = {"sequences": seqs, "rows": int(len(rows)), "max_abs_err": float(err.max()),
+                         "bound": "|gpu - ref| <= 0.002 + 0.01 |ref| per element",
+                         "within_bound": bool(np.all(err <= 2e-3 + 1e-2 * np.abs(ref)))}
+    del w, out, dec
+    torch.cuda.empty_cache()
+    return res
+
+
+def shared_prefix_measure(n: int, dev, B, evict) -> dict:
+    """Shared-prefix decode on parallel_sampling (32 prompts x 4 samples): the
+    call that reads each group's shared prompt blocks once, timed as a CUDA
+    graph against plain decode of the same batch, and checked against the
+    oracle on every sequence and head."""
+    import oracle
+    sp = W.spec("parallel_sampling")
+    w = W.make_workload(sp, device=dev)
+    lay = w.layout
+    host = {k: W.to_numpy(getattr(w, k)) for k in ("q", "k_cache", "v_cache", "k_new", "v_new")}
+    H = sp.num_q_heads
+    groups = torch.from_numpy(lay.group_members).to(dev)
+    shared = torch.from_numpy(lay.shared_blocks).to(dev)
+    out_c, out_p = torch.empty_like(w.q), torch.empty_like(w.q)
+    maxlen = lay.max_context_len
+    ws_c = torch.empty(B.shared_prefix_workspace_bytes(sp.num_seqs, H, sp.head_dim, maxlen, groups.shape[1]),
+                       dtype=torch.uint8, device=dev)
+    ws_p = torch.zeros(max(16, B.workspace_bytes(sp.num_seqs, H, sp.num_kv_heads, sp.head_dim, maxlen)),
+                       dtype=torch.uint8, device=dev)
+    # the step's writes, in the step's order: copy-on-write copies, then the new tokens
+    B.copy_blocks(w.k_cache, w.v_cache, w.cow_pairs, host_pairs=lay.cow_pairs)
+    B.kv_append(w.k_new, w.v_new, w.slot_mapping, w.k_cache, w.v_cache)
+    t_c = graph_time(lambda: B.paged_decode_attention_shared_prefix(
+        out_c, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, groups, shared,
+        max_context_len=maxlen, workspace=ws_c), n, dev, evict)
+    t_p = graph_time(lambda: B.paged_decode_attention(
+        out_p, w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, w.scale, max_context_len=maxlen,
+        workspace=ws_p), n, dev, evict)
+    torch.cuda.synchronize(dev)
+    if B.device_error(clear=True):
+        raise RuntimeError("device error word set during the shared-prefix benchmark")
+    oracle.copy_blocks(host["k_cache"], host["v_cache"], lay.cow_pairs)
+    oracle.kv_append(host["k_new"], host["v_new"], lay.slot_mapping, host["k_cache"], host["v_cache"])
+    ref = oracle.paged_decode_attention(host["q"], host["k_cache"], host["v_cache"], lay.block_tables,
+                                        lay.context_lens, w.scale, sp.num_kv_heads, nthreads=cpu_cores())
+    got = out_c.float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)
+    eb = 2
+    logical, unique = lay.kv_bytes(eb), lay.unique_kv_bytes(eb)
+    peak, kind = peaks()
+    res = {"workload": describe(sp), "groups": int(groups.shape[0]), "shared_blocks": int(lay.shared_blocks[0]),
+           "shared_prefix": {"us": round(t_c * 1e6, 2), "logical_GBps": round(logical / t_c / 1e9, 2),
+                             "unique_GBps": round(unique / t_c / 1e9, 2),
+                             "unique_frac_of_peak": round(unique / t_c / 1e9 / peak, 4)},
+           "plain_decode": {"us": round(t_p * 1e6, 2), "logical_GBps": round(logical / t_p / 1e9, 2)},
+           "speedup": round(t_p / t_c, 3), "logical_bytes": int(logical), "unique_bytes": int(unique),
+           "parity": {"sample_seqs": int(sp.num_seqs), "max_abs_err": float(err.max()),
+                      "bound": "|gpu - ref| <= 0.002 + 0.01 |ref| per element",
+                      "within_bound": bool(np.all(np.isfinite(got)) and np.all(err <= 2e-3 + 1e-2 * np.abs(ref)))},
+           "peak": peak, "peak_kind": kind}
+    del w, out_c, out_p, ws_c, ws_p
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_prefill(args, dev, B):
+    evict = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev).fill_(1.0)
+    res = prefill_measure(args.prefill_workload, args.steps or 30, dev, B, evict)
     line = {"metric": "prefill attention TFLOP/s (causal, algorithmic FLOPs)", "unit": "TFLOP/s",
-            "value": round(tflops, 2), "tokens_per_s": round(T / t_step, 1),
-            "attention": {"us": round(t_attn * 1e6, 2), "TFLOP/s": round(tflops, 2),
-                          "frac_of_peak": round(tflops / peak, 4)},
-            "step": {"us": round(t_step * 1e6, 2), "what": "kv_append of every new token + prefill attention"},
-            "flops": int(flops), "new_tokens": T, "peak": peak, "peak_kind": kind, "bound": "tensor",
-            "check": {"last_rows_vs_decode_max_abs_diff": diff, "rows": int(len(has))},
-            "higher_is_better": True,
+            "value": res["attention"]["TFLOP/s"], "tokens_per_s": res["step"]["tokens_per_s"],
+            "attention": res["attention"], "step": res["step"], "flops": res["flops"],
+            "new_tokens": res["new_tokens"], "bound": "tensor", "check": res["check"], "higher_is_better": True,
             "timing": "each variant captured once as a CUDA graph, median of replays after an L2 eviction",
-            "config": {"workload": f"{sp.name}: {sp.num_seqs} seqs, {sp.num_q_heads} q / {sp.num_kv_heads} kv "
-                                   f"heads, head_dim {sp.head_dim}, bf16, block 16, new tokens {sp.new_lengths} "
-                                   f"[{sp.new_lo}, {sp.new_hi}], prior context [{sp.prior_lo}, {sp.prior_hi}]"},
-            "op": "prefill", "n_gpus": 1, "dtype": "bf16", "data": "synthetic"}
+            "config": {"workload": res["workload"]}, "op": "prefill", "n_gpus": 1, "dtype": "bf16",
+            "data": "synthetic"}
     print(json.dumps(line), flush=True)
 
 
