@@ -102,16 +102,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
 constexpr int kRankMaxSeqs = 128;  // batches up to this size can be issued longest-first
 
 // The sequence a CTA with sequence rank z works on: in batches of up to
-// kRankMaxSeqs sequences, the z-th by new-token count (most first, ties by
-// index); larger batches in index order. Warp 0 ranks the counts from
-// shared memory; every thread of the CTA calls it (it holds a barrier).
+// kRankMaxSeqs sequences, the z-th by context length (longest first, ties by
+// index: with chunks after a long cached context a CTA's work grows with the
+// context, so the longest CTAs start first); larger batches in index order.
+// Warp 0 ranks the lengths from shared memory; every thread of the CTA calls
+// it (it holds a barrier).
 __device__ __forceinline__ int prefill_sequence_by_rank(const PrefillParams &pp, int z, int tid) {
     const int S = pp.d.num_seqs;
     if (S > kRankMaxSeqs) return z;
     __shared__ int counts[kRankMaxSeqs];
     __shared__ int chosen;
     if (tid < 32) {
-        for (int i = tid; i < S; i += 32) counts[i] = __ldg(pp.query_start + i + 1) - __ldg(pp.query_start + i);
+        for (int i = tid; i < S; i += 32) counts[i] = seq_len(pp.d, i, false);
         __syncwarp();
         for (int i = tid; i < S; i += 32) {
             const int ni = counts[i];
@@ -139,7 +141,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
     //  - grid (kv heads, sequences, pairs), the pair index slowest and taken from the
     //    last: every sequence's longest pairs start first and the short ones fill the end;
     //  - grid (kv heads, pairs, sequence rank): one sequence at a time, sequences in
-    //    decreasing order of new tokens, each one's longest pairs first over its kv heads;
+    //    decreasing order of context length, each one's longest pairs first over its kv heads;
     //    a (sequence, kv head)'s pairs start num_kv_heads CTAs apart, so they read its
     //    K/V while it is in L2 without streaming it in lockstep.
     const int h = blockIdx.x;

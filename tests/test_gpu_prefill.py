@@ -167,7 +167,7 @@ def test_long_prefix_chunks_sampled():
 def test_cta_order_does_not_change_the_result(num_seqs):
     """The grid is issued pair index slowest when the contexts are not much
     longer than the new tokens, else one sequence at a time in decreasing order
-    of new tokens (ranked inside the kernel for batches of up to 128 sequences,
+    of context length (ranked inside the kernel for batches of up to 128 sequences,
     in index order beyond). A larger host bound on the context length selects
     the second order for the same inputs: the outputs are bit-identical, and
     match the oracle. Lengths repeat, so the ranking meets ties."""
