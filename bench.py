@@ -98,24 +98,26 @@ PROFILED = {
 }
 _CSRC = "paged_kv_cache_177_gb300/csrc/"
 _DEVICE_COMMON = ["kBlock", "kSplitBlocks", "g_dev_error", "raise_error", "to_out", "DecodeParams", "seq_len",
-                  "WarpAttn"]
-_HOST_COMMON = ["PKV_GRID_STAGES", "PKV_GRID_CONSUMERS", "PKV_PERSIST_WARPS", "PKV_PERSIST_STAGES_D128",
-                "PKV_PERSIST_STAGES_D64", "PKV_PERSIST_MAX_SEQS", "PKV_MHA_CUDA_CORES", "kCounterBytes", "kPersistWarps", "kPersistMaxCtas", "kPersistMaxSeqs", "kNstage", "kNcw",
-                "kSmemLimit", "launch_pdl", "encode_fn", "encode_cache_map", "max_parts_for", "sm_count",
-                "decode_dispatch", "pkv_decode_partition_tokens", "pkv_decode_workspace_bytes",
-                "grid_workspace_bytes", "persist_workspace_bytes", "input_dtype", "use_persistent"]
+                  "WarpAttn", "WarpAttnScalar"]
+_HOST_COMMON = ["PKV_MHA_CUDA_CORES", "kMhaCudaCores", "kCounterBytes", "kSmemLimit", "launch_pdl", "encode_fn",
+                "encode_cache_map", "max_parts_for", "sm_count", "decode_dispatch", "pkv_decode_partition_tokens",
+                "pkv_decode_workspace_bytes", "grid_workspace_bytes", "input_dtype", "use_persistent"]
 KERNEL_SPANS = {
     "decode_bf16_persistent_kernel": {
         "include/pagedkv.h": None, _CSRC + "pkv_ptx.cuh": None,
-        _CSRC + "pkv_kernels.cuh": _DEVICE_COMMON + ["WarpAttnScalar", "PersistCfg", "Cursor", "cursor_advance",
-                                                     "merge_segments", "decode_bf16_persistent_kernel"],
-        _CSRC + "pkv.cu": _HOST_COMMON + ["kMhaCudaCores", "launch_persistent", "persistent_by_shape"],
+        _CSRC + "pkv_kernels.cuh": _DEVICE_COMMON + ["PersistCfg", "Cursor", "cursor_advance", "merge_segments",
+                                                     "decode_bf16_persistent_kernel"],
+        _CSRC + "pkv.cu": _HOST_COMMON + ["PKV_PERSIST_WARPS", "PKV_PERSIST_STAGES_D128", "PKV_PERSIST_STAGES_D64",
+                                          "PKV_PERSIST_MAX_SEQS", "kPersistWarps", "kPersistMaxCtas",
+                                          "kPersistMaxSeqs", "persist_workspace_bytes", "launch_persistent",
+                                          "persistent_by_shape"],
     },
     "decode_bf16_kernel": {
         "include/pagedkv.h": None, _CSRC + "pkv_ptx.cuh": None,
         _CSRC + "pkv_kernels.cuh": _DEVICE_COMMON + ["Bf16Cfg", "grid_produce", "grid_consume",
                                                      "decode_bf16_kernel", "block_reduce", "lse_reduce_kernel"],
-        _CSRC + "pkv.cu": _HOST_COMMON + ["launch_bf16", "grid_by_shape", "launch_reduce"],
+        _CSRC + "pkv.cu": _HOST_COMMON + ["PKV_GRID_STAGES", "PKV_GRID_CONSUMERS", "kNstage", "kNcw",
+                                          "launch_bf16", "grid_by_shape", "launch_reduce"],
     },
 }
 

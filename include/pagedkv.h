@@ -111,7 +111,7 @@ int pkv_version(void);
  *
  * bf16 has a second decomposition, chosen with PKV_PARTITION_BALANCED, or
  * automatically (partition_tokens == 0) when the batch has at least a quarter
- * as many (sequence, kv head) pairs as the GPU runs persistent warps (16 per
+ * as many (sequence, kv head) pairs as the GPU runs persistent warps (12 per
  * SM): the blocks of all pairs are cut into equal shares, one per warp of a
  * persistent kernel (one CTA per SM), and the pieces of a cut sequence are
  * merged with the same log-sum-exp rule inside that kernel. Batches of a few

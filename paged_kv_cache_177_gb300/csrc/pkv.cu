@@ -29,7 +29,7 @@ constexpr int kMaxParts = 8192;        // partitions per sequence the reduce ker
 #define PKV_GRID_CONSUMERS 4
 #endif
 #ifndef PKV_PERSIST_WARPS
-#define PKV_PERSIST_WARPS 16
+#define PKV_PERSIST_WARPS 12
 #endif
 #ifndef PKV_PERSIST_STAGES_D128
 #define PKV_PERSIST_STAGES_D128 1

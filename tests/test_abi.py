@@ -64,16 +64,16 @@ def test_partition_and_workspace_sizing(binding):
     assert binding.workspace_bytes(8, 64, 8, 128, 131072, 512) == hdr + 8 * 64 * 256 * 130 * 4
     assert binding.workspace_bytes(2, 4, 4, 64, 1000, 64) == hdr + 2 * 4 * 16 * 66 * 4
     # the persistent layout does not depend on the batch size: one state per
-    # group head for two segments of each of up to 160 x 16 workers
+    # group head for two segments of each of up to 160 x 12 workers
     for S in (1, 64, 8192):
-        assert binding.workspace_bytes(S, 32, 8, 128, 64, -1) == hdr + 160 * 16 * 2 * 4 * 130 * 4
+        assert binding.workspace_bytes(S, 32, 8, 128, 64, -1) == hdr + 160 * 12 * 2 * 4 * 130 * 4
 
 
 def test_counter_header_size_matches_the_header():
     from paged_kv_cache_177_gb300 import binding as b
     m = re.search(r"#define\s+PKV_DECODE_COUNTER_BYTES\s+(\d+)u?", open(HEADER).read())
     assert m and int(m.group(1)) == b.DECODE_COUNTER_BYTES
-    assert b.DECODE_COUNTER_BYTES % 256 == 0 and b.DECODE_COUNTER_BYTES >= 160 * 16 * 4
+    assert b.DECODE_COUNTER_BYTES % 256 == 0 and b.DECODE_COUNTER_BYTES >= 160 * 12 * 4
 
 
 def test_which_decode_kernel_runs(binding):
