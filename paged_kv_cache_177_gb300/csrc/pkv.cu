@@ -42,6 +42,10 @@ constexpr int kMaxParts = 8192;        // partitions per sequence the reduce ker
 #endif
 constexpr int kNstage = PKV_GRID_STAGES;
 constexpr bool kMhaCudaCores = PKV_MHA_CUDA_CORES != 0;  // g = 1 on the CUDA cores (persistent kernel)
+#ifndef PKV_PREFILL_UNITS
+#define PKV_PREFILL_UNITS 1
+#endif
+constexpr bool kPrefillUnits = PKV_PREFILL_UNITS != 0;  // prefill: one CTA per (sequence, kv head) when many
 
 constexpr int kNcw = PKV_GRID_CONSUMERS;
 // persistent bf16 kernel: one CTA of kPersistWarps warps per SM
@@ -210,12 +214,12 @@ int launch_reduce(const pkv::DecodeParams &p, pkv_dtype dt, cudaStream_t st) {
 }
 
 
-template <int D>
+template <int D, bool kUnits>
 int launch_prefill_tc(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMap &tmv,
                       const pkv::PrefillParams &pp, dim3 grid, cudaStream_t st) {
     using C = pkv::TcCfg<D>;
     static_assert(C::kSmem <= (int)kSmemLimit, "shared memory");
-    auto kern = pkv::prefill_tc_kernel<D>;
+    auto kern = kUnits ? pkv::prefill_tc_units_kernel<D> : pkv::prefill_tc_kernel<D>;
     static thread_local int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -704,14 +708,24 @@ int paged_prefill_attention(void *out, const void *q, const void *k_cache, const
     // (sequence, kv head) read its K/V from L2 -- there each pair attends the
     // whole cached context, and re-reading it from DRAM dominates.
     pp.seq_major = max_context_len >= 2 * max_query_len ? 1 : 0;
-    const dim3 grid = pp.seq_major ? dim3(num_kv_heads, pairs, num_seqs) : dim3(num_kv_heads, num_seqs, pairs);
+    // Many (sequence, kv head) units of whole prompts: one CTA per unit takes all its pairs, so
+    // each CTA's set-up is paid once and the next pair's loads overlap the current pair's end.
+    int sms = 0;
+    if (sm_count(&sms) != PKV_OK) return PKV_ERR_CUDA;
+    const bool units = kPrefillUnits && !pp.seq_major && (long long)num_seqs * num_kv_heads >= 4LL * sms;
+    const dim3 grid = units          ? dim3(num_kv_heads, num_seqs)
+                      : pp.seq_major ? dim3(num_kv_heads, pairs, num_seqs)
+                                     : dim3(num_kv_heads, num_seqs, pairs);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     alignas(64) CUtensorMap tmq;
     if ((rc = encode_q_map(&tmq, q, num_queries, num_q_heads, head_dim, g, tile_tokens)) != PKV_OK) return rc;
     if ((rc = encode_cache_map(&tmk, k_cache, num_blocks, num_kv_heads, head_dim, true)) != PKV_OK) return rc;
     if ((rc = encode_cache_map(&tmv, v_cache, num_blocks, num_kv_heads, head_dim, true)) != PKV_OK) return rc;
-    return head_dim == 128 ? launch_prefill_tc<128>(tmq, tmk, tmv, pp, grid, st)
-                           : launch_prefill_tc<64>(tmq, tmk, tmv, pp, grid, st);
+    if (units)
+        return head_dim == 128 ? launch_prefill_tc<128, true>(tmq, tmk, tmv, pp, grid, st)
+                               : launch_prefill_tc<64, true>(tmq, tmk, tmv, pp, grid, st);
+    return head_dim == 128 ? launch_prefill_tc<128, false>(tmq, tmk, tmv, pp, grid, st)
+                           : launch_prefill_tc<64, false>(tmq, tmk, tmv, pp, grid, st);
 }
 
 int pkv_check_copy_pairs(const int64_t *host_pairs, int num_pairs, int num_blocks) {
