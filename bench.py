@@ -464,7 +464,7 @@ def config_summary(name: str, args, dev, B, evict) -> dict:
     gbs, secs, nseq, passes, sb = oracle_sample(lay, host, args.config_cpu_seconds)
     parity = full_parity(lay, host, out, sp.dtype, out32)
     kernel = ("decode_bf16_persistent_kernel" if persistent else
-              ("decode_bf16_kernel" if sp.dtype == "bf16" else "decode_f32_kernel") +
+              ("decode_bf16_kernel" if sp.dtype == "bf16" else "decode_f32_staged_kernel") +
               (" + lse_reduce_kernel" if launches == 2 else ""))
     res = {
         "workload": describe(sp),
@@ -760,7 +760,7 @@ def run_ours(args, rank, world, local, dist):
                                  for name in W.PREFILL_SPECS}}
     srt = sorted(step_ms)
     roof_kernel = ("decode_bf16_persistent_kernel" if persistent else
-                   "decode_bf16_kernel" if sp.dtype == "bf16" else "decode_f32_kernel")
+                   "decode_bf16_kernel" if sp.dtype == "bf16" else "decode_f32_staged_kernel")
     # the captures were taken on the workloads' default launch configuration
     traffic, traffic_src = profiled_traffic(sp.name if args.partition_tokens is None and args.dtype is None else "",
                                             roof_kernel)

@@ -130,6 +130,22 @@ int encode_cache_map(CUtensorMap *map, const void *cache, int num_blocks, int nu
 // (one_half: a box of one 64-element half of the 16 slots' rows, 2 KiB, so a
 // caller can place the halves of consecutive blocks apart.)
 
+// The same view of an fp32 cache: x = element within a 32-element (128-byte) quarter
+// or half row, z = which one (head_dim / 32). The box {32, 16, head_dim / 32, 1} is the
+// whole tile, landing as [sub-tile][slot][32] with the 128-byte swizzle.
+int encode_cache_map_f32(CUtensorMap *map, const void *cache, int num_blocks, int num_kv_heads, int head_dim) {
+    auto fn = encode_fn();
+    if (!fn) return PKV_ERR_CUDA;
+    cuuint64_t dims[4] = {32, 16, (cuuint64_t)head_dim / 32, (cuuint64_t)num_blocks * num_kv_heads};
+    cuuint64_t strides[3] = {(cuuint64_t)head_dim * 4, 128, (cuuint64_t)head_dim * 4 * 16};
+    cuuint32_t box[4] = {32, 16, (cuuint32_t)head_dim / 32, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(cache), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
 // 4-D view of q [T][Hq][D] for the tensor-core prefill: x = element within a
 // 64-element half row, y = half, z = query head, w = query row (token). The
 // box {64, 1, g, tokens} lands one half of a (token, head) tile as rows
@@ -171,13 +187,49 @@ int launch_bf16(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::Decod
     return check_launch();
 }
 
-template <int D>
-int launch_f32(const pkv::DecodeParams &p, dim3 grid, cudaStream_t st, bool pdl = false) {
-    // every warp's per-head states, then the group's query rows
-    const size_t smem = ((size_t)kNcw * p.group * (D + 2) + (size_t)p.group * D) * sizeof(float);
-    if (pdl) return launch_pdl(pkv::decode_f32_kernel<D, kNcw>, grid, dim3(kNcw * 32), smem, st, p);
-    pkv::decode_f32_kernel<D, kNcw><<<grid, kNcw * 32, smem, st>>>(p);
+
+// fp32 caches: the staged kernel with the query-head bound GMAX >= g, four stages (a
+// stage is 16 KiB at d = 128).
+#ifndef PKV_F32_STAGES
+#define PKV_F32_STAGES 4
+#endif
+#ifndef PKV_F32_NCW
+#define PKV_F32_NCW 4
+#endif
+constexpr int kF32Stages = PKV_F32_STAGES, kF32Ncw = PKV_F32_NCW;
+
+template <int D, int GMAX>
+int launch_f32_staged(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, dim3 grid,
+                      cudaStream_t st, bool pdl) {
+    using C = pkv::F32Cfg<D, GMAX, kF32Stages, kF32Ncw>;
+    static_assert(C::kSmem <= (int)kSmemLimit, "shared memory");
+    auto kern = pkv::decode_f32_staged_kernel<D, GMAX, kF32Stages, kF32Ncw>;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (configured_device != dev) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured_device = dev;
+    }
+    if (pdl) return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmem, st, tmk, tmv, p);
+    kern<<<grid, C::kThreads, C::kSmem, st>>>(tmk, tmv, p);
     return check_launch();
+}
+
+// fp32 caches: the tensor maps of both caches, then the instance for the group size.
+template <int D>
+int launch_f32(const pkv::DecodeParams &p, dim3 grid, cudaStream_t st, bool pdl) {
+    alignas(64) CUtensorMap tmk, tmv;
+    int rc;
+    if ((rc = encode_cache_map_f32(&tmk, p.k_cache, p.num_blocks, p.num_kv_heads, D)) != PKV_OK) return rc;
+    if ((rc = encode_cache_map_f32(&tmv, p.v_cache, p.num_blocks, p.num_kv_heads, D)) != PKV_OK) return rc;
+    const int g = p.group;
+    if (g == 1) return launch_f32_staged<D, 1>(tmk, tmv, p, grid, st, pdl);
+    if (g == 2) return launch_f32_staged<D, 2>(tmk, tmv, p, grid, st, pdl);
+    if (g <= 4) return launch_f32_staged<D, 4>(tmk, tmv, p, grid, st, pdl);
+    if (g <= 8) return launch_f32_staged<D, 8>(tmk, tmv, p, grid, st, pdl);
+    return launch_f32_staged<D, 16>(tmk, tmv, p, grid, st, pdl);
 }
 
 template <int D, int NT>

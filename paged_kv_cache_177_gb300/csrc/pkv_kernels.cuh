@@ -1,7 +1,7 @@
 // pkv_kernels.cuh -- device code of the PagedAttention decode library.
 //
 // K1 decode_bf16_kernel   block-table gather (TMA) + QK^T + online softmax + PV on tensor cores
-// K1 decode_f32_kernel    the same step in fp32 on the CUDA cores (exact-precision path)
+// K1 decode_f32_staged_kernel  the same step for fp32 caches on the CUDA cores (exact-precision path)
 // K2 lse_reduce_kernel    merges split-context partitions with a log-sum-exp reduce
 // K3 kv_append_kernel     slot-mapped write of new tokens' K/V
 // K4 move_blocks_kernel   whole-block copies: copy-on-write, swap to/from a host pool, several layers
@@ -1403,25 +1403,233 @@ struct PrefillParams {
 };
 
 // =====================================================================================
-// K1 (fp32): same decomposition on the CUDA cores, for fp32 caches where the
-// result must hold to ~1e-5. One CTA per (partition, kv head, sequence); warp w
-// takes blocks w, w+NCW, ...; lane l owns head-dim elements l, l+32, ...
-// Eight tokens at a time: their K and V rows stay in registers while every
-// query head of the group attends them (each K/V element read once). For one
-// head, the lanes' partial dot products of the 8 tokens are summed by a
-// transpose-reduce (9 shuffles; lane 4 t ends with token t's full sum), then
-// the online update over the 8 scores x_t = scale log2(e) <q, K_t>:
-//   m' = max(m, max_t x_t), l = l 2^(m-m') + sum_t 2^(x_t-m'),
-//   acc = acc 2^(m-m') + sum_t 2^(x_t-m') V_t.
-// Each head's (m, l, acc) lives in shared memory between passes.
+// K1 (fp32, staged): the grid kernel's decomposition for fp32 caches. Warp NCW stages
+// each (block, kv head) K and V tile -- [16 tokens][D] fp32, contiguous in HBM -- by TMA
+// into an NSTAGE ring, as D / 32 sub-tiles of 16 rows x 128 bytes with the 128-byte
+// swizzle; warps 0..NCW-1 (alone, or in teams of two that split a block's query heads)
+// run WarpAttnF32 on the CUDA cores over their blocks and merge their states through
+// shared memory. The group's query rows are staged in shared memory once per CTA.
 // =====================================================================================
-// Five CTAs per SM (at most 96 registers per thread, no spills): more warps hide more of
-// the load latency (measured: GQA batches 5-9% faster, 13B-class MHA within 1%).
-template <int D, int NCW>
-__global__ void __launch_bounds__(NCW * 32, 5) decode_f32_kernel(const DecodeParams p) {
-    pdl_wait();  // the caches may have been written by the previous kernel (kv_append in a decode step)
-    constexpr int PER = D / 32;
-    extern __shared__ float fsm[];  // per-warp head states (also the merge buffer) [NCW][g][D + 2], q [g][D]
+// Query-head bound from which two warps share each block (each half the heads).
+#ifndef PKV_F32_SPLIT_FROM
+#define PKV_F32_SPLIT_FROM 4
+#endif
+
+template <int D, int GMAX, int NSTAGE, int NCW>
+struct F32Cfg {
+    static constexpr int kSubBytes = kBlock * 128;               // 2 KiB: 16 rows of 32 fp32
+    static constexpr int kTile = kBlock * D * 4;                 // one (block, head) tile of K or V
+    static constexpr int kStage = 2 * kTile;                     // K tile + V tile
+    static constexpr int kThreads = (NCW + 1) * 32;
+    static constexpr int kSplit = GMAX >= PKV_F32_SPLIT_FROM ? 2 : 1;  // warps sharing a block (each half the heads)
+    static constexpr int kTeams = NCW / kSplit;
+    static constexpr int kWarpHeads = GMAX / kSplit;             // query-head bound of one warp
+    static constexpr int kMergeStride = D + 4;
+    static constexpr int kMergeBytes = NCW * kWarpHeads * (2 + kMergeStride) * 4;
+    static constexpr int kQuarterBytes = D + 16;                 // a quarter row of q (D / 4 fp32) + 16 bytes
+    static constexpr int kQRow = 4 * kQuarterBytes;
+    static constexpr int kPBytes = kWarpHeads * kBlock * 4;      // one warp's weights of a block
+    static constexpr int kBarOffset = NSTAGE * kStage;
+    static constexpr int kQOffset = kBarOffset + 2 * NSTAGE * 8;
+    static constexpr int kPOffset = kQOffset + GMAX * kQRow;
+    static constexpr int kSmem = kPOffset + NCW * kPBytes + 1024;  // + slack for 1 KiB alignment
+    static_assert(kMergeBytes <= kBarOffset, "merge buffer must fit in the stage ring");
+    static_assert(NCW % kSplit == 0 && NSTAGE % kTeams == 0, "each stage is always consumed by the same team");
+    static_assert(kQOffset % 16 == 0, "16-byte loads of the staged q");
+};
+
+// One warp's online-softmax state for g <= GMAX query heads of a kv head (all of the
+// group's, or one warp's share of them), over fp32 K/V tiles staged as F32Cfg lays them out. Scores: lane (quarter h4 = lane / 8,
+// token t8 = lane % 8) dots its quarter of the head dimension for tokens t8 and t8 + 8
+// with every head's query (packed fp32 pairs), then two shuffles add the quarters. The
+// softmax weights go through the warp's shared-memory slot so that P V can take four
+// tokens' weights of a head in one broadcast load; lane l accumulates head-dim elements
+// kDims l .. kDims l + kDims - 1 of every head.
+template <int D, int GMAX>
+struct WarpAttnF32 {
+    static constexpr int kQC = D / 16;        // 16-byte chunks in a quarter row
+    static constexpr int kDims = D / 32;      // output elements per lane (4 or 2)
+    static constexpr int kQuarterBytes = D + 16;
+    static constexpr int kQRow = 4 * kQuarterBytes;
+    static constexpr int kHG = GMAX <= 4 ? GMAX : 4;  // heads per group
+    float m[GMAX], l[GMAX];
+    uint64_t acc[GMAX][kDims / 2];
+    uint32_t q_s, p_s;  // shared addresses: staged query rows, this warp's weights
+    int g;
+
+    __device__ __forceinline__ void init(uint32_t q_smem, uint32_t p_smem, int group) {
+        q_s = q_smem;
+        p_s = p_smem;
+        g = group;
+    }
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+#pragma unroll
+            for (int i = 0; i < kDims / 2; ++i) acc[h][i] = 0;
+        }
+    }
+
+    // Rows below `lo` of the staged tiles are not tokens of the sequence (zero-filled by TMA).
+    // Heads go in groups of kHG (scores, softmax, then P V per group): fewer registers at
+    // the price of reading the block's K and V tiles from shared memory once per group.
+    __device__ __forceinline__ void block(uint32_t sk, uint32_t sv, int lo, float scale_log2, int lane, int = 0,
+                                          int = 0, bool = false) {
+        const int h4 = lane >> 3, t8 = lane & 7;
+        constexpr int kLaneBytes = kDims * 4;
+        const int ci_v = (lane * kLaneBytes) >> 4;
+        const uint32_t vbase = sv + (ci_v >> 3) * (kBlock * 128) + ((lane * kLaneBytes) & 15);
+        const int cv = ci_v & 7;
+#pragma unroll
+        for (int hg = 0; hg < GMAX; hg += kHG) {
+            if (hg >= g) break;
+            uint64_t da[kHG], db[kHG];  // partial dot products, tokens t8 and t8 + 8
+#pragma unroll
+            for (int k = 0; k < kHG; ++k) da[k] = db[k] = 0;
+#pragma unroll
+            for (int j = 0; j < kQC; ++j) {
+                const int ci = h4 * kQC + j;  // 16-byte chunk of the row
+                const int u = ci >> 3, c = ci & 7;
+                const uint32_t at = sk + u * (kBlock * 128) + ((c ^ t8) << 4);  // rows t8, t8 + 8 share the swizzle
+                uint32_t x[4], y[4];
+                ld_shared_v4(at + t8 * 128, x);
+                ld_shared_v4(at + (t8 + 8) * 128, y);
+                const uint64_t x01 = pack_f2(__uint_as_float(x[0]), __uint_as_float(x[1]));
+                const uint64_t x23 = pack_f2(__uint_as_float(x[2]), __uint_as_float(x[3]));
+                const uint64_t y01 = pack_f2(__uint_as_float(y[0]), __uint_as_float(y[1]));
+                const uint64_t y23 = pack_f2(__uint_as_float(y[2]), __uint_as_float(y[3]));
+#pragma unroll
+                for (int k = 0; k < kHG; ++k) {
+                    if (hg + k < g) {
+                        uint32_t qv[4];
+                        ld_shared_v4(q_s + (hg + k) * kQRow + h4 * kQuarterBytes + j * 16, qv);
+                        const uint64_t q01 = pack_f2(__uint_as_float(qv[0]), __uint_as_float(qv[1]));
+                        const uint64_t q23 = pack_f2(__uint_as_float(qv[2]), __uint_as_float(qv[3]));
+                        da[k] = fma_f2(x23, q23, fma_f2(x01, q01, da[k]));
+                        db[k] = fma_f2(y23, q23, fma_f2(y01, q01, db[k]));
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kHG; ++k) {
+                const int h = hg + k;
+                if (h < g) {
+                    float a0, a1, b0, b1;
+                    unpack_f2(da[k], a0, a1);
+                    unpack_f2(db[k], b0, b1);
+                    float s0 = a0 + a1, s1 = b0 + b1;
+                    s0 += __shfl_xor_sync(0xffffffffu, s0, 8);
+                    s1 += __shfl_xor_sync(0xffffffffu, s1, 8);
+                    s0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+                    s1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+                    const float x0 = t8 >= lo ? s0 * scale_log2 : -INFINITY;
+                    const float x1 = t8 + 8 >= lo ? s1 * scale_log2 : -INFINITY;
+                    float mx = fmaxf(x0, x1);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    const float mn = fmaxf(m[h], mx);        // finite: a block holds at least one token
+                    const float al = ex2_approx(m[h] - mn);  // 0 on the first block (m = -inf)
+                    const float p0 = ex2_approx(x0 - mn), p1 = ex2_approx(x1 - mn);
+                    m[h] = mn;
+                    l[h] = l[h] * al + (h4 == 0 ? p0 + p1 : 0.f);
+                    const uint64_t al2 = pack_f2(al, al);
+#pragma unroll
+                    for (int i = 0; i < kDims / 2; ++i) acc[h][i] = fma_f2(acc[h][i], al2, 0);
+                    if (h4 == (k & 3)) {  // one quarter of the lanes writes the head's weights
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(p_s + (h * kBlock + t8) * 4), "f"(p0) : "memory");
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(p_s + (h * kBlock + t8 + 8) * 4), "f"(p1)
+                                     : "memory");
+                    }
+                }
+            }
+            __syncwarp();
+            // P V: this lane's kDims elements of every token's V row, the group's heads
+#pragma unroll
+            for (int t4 = 0; t4 < kBlock; t4 += 4) {
+                float pw[kHG][4];
+#pragma unroll
+                for (int k = 0; k < kHG; ++k) {
+                    if (hg + k < g) {
+                        uint32_t w[4];
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                                     : "r"(p_s + ((hg + k) * kBlock + t4) * 4)
+                                     : "memory");
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) pw[k][e] = __uint_as_float(w[e]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = t4 + e;
+                    const uint32_t at = vbase + t * 128 + ((cv ^ (t & 7)) << 4);
+                    uint64_t v2[kDims / 2];
+                    if constexpr (kDims == 4) {
+                        uint32_t w[4];
+                        ld_shared_v4(at, w);
+                        v2[0] = pack_f2(__uint_as_float(w[0]), __uint_as_float(w[1]));
+                        v2[1] = pack_f2(__uint_as_float(w[2]), __uint_as_float(w[3]));
+                    } else {
+                        uint32_t w[2];
+                        ld_shared_v2(at, w);
+                        v2[0] = pack_f2(__uint_as_float(w[0]), __uint_as_float(w[1]));
+                    }
+#pragma unroll
+                    for (int k = 0; k < kHG; ++k) {
+                        if (hg + k < g) {
+                            const uint64_t p2 = pack_f2(pw[k][e], pw[k][e]);
+#pragma unroll
+                            for (int i = 0; i < kDims / 2; ++i) acc[hg + k][i] = fma_f2(v2[i], p2, acc[hg + k][i]);
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();  // the weights' slot is rewritten by the next block
+    }
+
+    __device__ __forceinline__ void reduce_l() {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h)
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], o);
+    }
+
+    // Rows h < GMAX of the merge buffer (rows past the warp's heads are never read).
+    __device__ __forceinline__ void store_merge(float *ml, float *acc_rows, int stride, int lane) const {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            if (lane == 0) {
+                ml[h * 2 + 0] = m[h];
+                ml[h * 2 + 1] = l[h];
+            }
+#pragma unroll
+            for (int i = 0; i < kDims / 2; ++i) {
+                float a, b;
+                unpack_f2(acc[h][i], a, b);
+                acc_rows[h * stride + kDims * lane + 2 * i] = a;
+                acc_rows[h * stride + kDims * lane + 2 * i + 1] = b;
+            }
+        }
+    }
+};
+
+// From a query-head bound of PKV_F32_SPLIT_FROM on, each block is split between the two
+// warps of a team (each takes half the heads on the same staged tiles): a block's
+// CUDA-core work is halved, and each team alternates between two stages, so a warp's
+// next block is in flight while it computes.
+template <int D, int GMAX, int NSTAGE, int NCW>
+__global__ void __launch_bounds__((NCW + 1) * 32, GMAX >= 16 ? 1 : (GMAX >= 8 ? 2 : 3))
+    decode_f32_staged_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                             const DecodeParams p) {
+    using C = F32Cfg<D, GMAX, NSTAGE, NCW>;
+    constexpr int GW = C::kWarpHeads;
+    extern __shared__ uint8_t smem_raw[];
+
     const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = p.group;
@@ -1429,133 +1637,94 @@ __global__ void __launch_bounds__(NCW * 32, 5) decode_f32_kernel(const DecodePar
     const int nblk = (len + kBlock - 1) / kBlock;
     const int npart = (nblk + p.part_blocks - 1) / p.part_blocks;
     float *out = static_cast<float *>(p.out);
-    if (len == 0) {
+
+    if (len == 0) {  // empty context: zero output rows
         if (part == 0) {
             float *o = out + ((size_t)s * p.num_q_heads + (size_t)h * g) * D;
-            for (int i = tid; i < g * D; i += NCW * 32) o[i] = 0.f;
+            for (int i = tid; i < g * D; i += C::kThreads) o[i] = 0.f;
         }
         return;
     }
     if (part >= npart) return;
+
     const int b_begin = part * p.part_blocks;
     const int nb = min(nblk - b_begin, p.part_blocks);
-    const int last_valid = len - (nblk - 1) * kBlock;
-    const float *kc = static_cast<const float *>(p.k_cache);
-    const float *vc = static_cast<const float *>(p.v_cache);
-    const int32_t *bt = p.block_tables + (size_t)s * p.max_blocks_per_seq + b_begin;
+    const int last_valid = len - (nblk - 1) * kBlock;  // tokens in the sequence's last block
 
-    // Per warp, every head's running state [m, l, acc[D]] lives in fsm (the merge buffer); the
-    // group's query rows sit after all warps' states. A block is taken 8 tokens at a time: their
-    // K and V rows stay in registers (lane: head-dim elements lane, lane + 32, ..) while every
-    // head of the group attends them, so each K/V element is read once.
-    float *st = fsm + (size_t)warp * g * (D + 2);
-    float *qs = fsm + (size_t)NCW * g * (D + 2);
-    for (int i = tid; i < g * D; i += NCW * 32)
-        qs[i] = __ldg(static_cast<const float *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)h * g) * D + i);
-    for (int n = 0; n < g; ++n) {
-#pragma unroll
-        for (int i = 0; i < PER; ++i) st[n * (D + 2) + 2 + lane + 32 * i] = 0.f;
-        if (lane == 0) {
-            st[n * (D + 2)] = -INFINITY;
-            st[n * (D + 2) + 1] = 0.f;
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + C::kBarOffset);
+    uint64_t *empty = full + NSTAGE;
+    if (tid == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], C::kSplit);
         }
+        mbar_fence_init();
+    }
+    // the group's query rows: quarter r of head row hh at q_smem + hh kQRow + r kQuarterBytes
+    const float *qg = static_cast<const float *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)h * g) * D;
+    for (int i = tid; i < g * (D / 4); i += C::kThreads) {  // 16-byte pieces
+        const int hh = i / (D / 4), k = i - hh * (D / 4);  // piece k of row hh: quarter k / (D / 16)
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(qg + (size_t)hh * D) + k);
+        *reinterpret_cast<float4 *>(base + C::kQOffset + hh * C::kQRow + (k / (D / 16)) * C::kQuarterBytes +
+                                    (k % (D / 16)) * 16) = v;
     }
     __syncthreads();
-    // After the transpose-reduce below lane L holds the dot product of token tok(L) of the 8:
-    // bits 2, 3, 4 of L are bits 0, 1, 2 of the token, so lane 4 t holds token t.
-    const int tok = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-    const bool b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
-    for (int j = warp; j < nb; j += NCW) {
-        const int pb = __ldg(bt + j);
-        const bool bad = pb < 0 || pb >= p.num_blocks;
-        if (bad && lane == 0) raise_error(PKV_DEVERR_BLOCK_ID);
-        const int valid = (b_begin + j == nblk - 1) ? last_valid : kBlock;
-        const size_t tile = bad ? 0 : ((size_t)pb * p.num_kv_heads + h) * kBlock * D;
-        for (int t0 = 0; t0 < valid; t0 += 8) {
-            float kx[8][PER], vx[8][PER];
-#pragma unroll
-            for (int tt = 0; tt < 8; ++tt)
-#pragma unroll
-                for (int i = 0; i < PER; ++i) {
-                    const bool in = !bad && t0 + tt < valid;
-                    kx[tt][i] = in ? __ldg(kc + tile + (size_t)(t0 + tt) * D + lane + 32 * i) : 0.f;
-                    vx[tt][i] = in ? __ldg(vc + tile + (size_t)(t0 + tt) * D + lane + 32 * i) : 0.f;
-                }
-            for (int n = 0; n < g; ++n) {
-                float *sn = st + n * (D + 2);
-                float part[8];
-#pragma unroll
-                for (int tt = 0; tt < 8; ++tt) {
-                    float d = 0.f;
-#pragma unroll
-                    for (int i = 0; i < PER; ++i) d = fmaf(qs[n * D + lane + 32 * i], kx[tt][i], d);
-                    part[tt] = d;
-                }
-                // transpose-reduce: 8 partial sums per lane -> one full sum per lane (9 shuffles)
-                float w4[4], w2[2];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float mine = b4 ? part[4 + k] : part[k], other = b4 ? part[k] : part[4 + k];
-                    w4[k] = mine + __shfl_xor_sync(0xffffffffu, other, 16);
-                }
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const float mine = b3 ? w4[2 + k] : w4[k], other = b3 ? w4[k] : w4[2 + k];
-                    w2[k] = mine + __shfl_xor_sync(0xffffffffu, other, 8);
-                }
-                float dot = (b2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4);
-                dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-                dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-                const float x = (t0 + tok < valid) ? dot * p.scale_log2 : -INFINITY;
-                float mx = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float m_old = sn[0], l_old = sn[1];
-                const float m_new = fmaxf(m_old, mx);  // finite: the 8 hold at least one token
-                const float al = exp2f(m_old - m_new);
-                const float pw = exp2f(x - m_new);
-                float ps = pw;  // the 8 weights' sum (each token once: reduce over bits 2-4 only)
-                ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-                ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-                ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-                float acc[PER];
-#pragma unroll
-                for (int i = 0; i < PER; ++i) acc[i] = sn[2 + lane + 32 * i] * al;
-#pragma unroll
-                for (int tt = 0; tt < 8; ++tt) {
-                    const float pt = __shfl_sync(0xffffffffu, pw, 4 * tt);
-#pragma unroll
-                    for (int i = 0; i < PER; ++i) acc[i] = fmaf(pt, vx[tt][i], acc[i]);
-                }
-                __syncwarp();  // every lane has read sn before it is overwritten
-#pragma unroll
-                for (int i = 0; i < PER; ++i) sn[2 + lane + 32 * i] = acc[i];
-                if (lane == 0) {
-                    sn[0] = m_new;
-                    sn[1] = l_old * al + ps;
-                }
-                __syncwarp();
-            }
-        }
+
+    if (warp == NCW) {
+        grid_produce<C, NSTAGE>(tmk, tmv, p.block_tables + (size_t)s * p.max_blocks_per_seq, b_begin, nb, nblk - 1,
+                                last_valid, p.num_blocks, p.num_kv_heads, h, base, full, empty, lane);
+        return;
     }
-    __syncthreads();
+    // team `team` takes blocks team, team + kTeams, ...; its member `mem` the heads
+    // mem GW .. mem GW + GW - 1 of the group
+    const int team = warp / C::kSplit, mem = warp % C::kSplit;
+    const int h0 = mem * GW;
+    const int nh = min(GW, g - h0);
+    WarpAttnF32<D, GW> wa;
+    wa.init(smem_u32(base + C::kQOffset + h0 * C::kQRow), smem_u32(base + C::kPOffset + warp * C::kPBytes), nh);
+    wa.reset();
+    const int last_in_range = (b_begin + nb - 1 == nblk - 1) ? nb - 1 : -1;
+    for (int j = team; j < nb; j += C::kTeams) {
+        const int st = j % NSTAGE;
+        if (!mbar_wait(&full[st], (j / NSTAGE) & 1)) {
+            raise_error(PKV_DEVERR_TIMEOUT);
+            break;
+        }
+        const uint32_t sk = smem_u32(base + st * C::kStage);
+        wa.block(sk, sk + C::kTile, j == last_in_range ? kBlock - last_valid : 0, p.scale_log2, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    wa.reduce_l();
+    named_barrier_sync(1, NCW * 32);  // every consumer is done with the stage ring
+    float *mml = reinterpret_cast<float *>(base);   // [NCW][GW][2]
+    float *macc = mml + NCW * GW * 2;                // [NCW][GW][kMergeStride]
+    wa.store_merge(mml + warp * GW * 2, macc + warp * GW * C::kMergeStride, C::kMergeStride, lane);
+    named_barrier_sync(1, NCW * 32);
+    const size_t orow0 = (size_t)s * p.num_q_heads + (size_t)h * g;
     for (int idx = tid; idx < g * D; idx += NCW * 32) {
-        const int n = idx / D, d = idx - n * D;
+        const int col = idx / D, d = idx - col * D;
+        const int cm = col / GW, k = col - cm * GW;  // the member holding the column, its row there
         float M = -INFINITY;
-        for (int w = 0; w < NCW; ++w) M = fmaxf(M, fsm[((size_t)w * g + n) * (D + 2)]);
+#pragma unroll
+        for (int t = 0; t < C::kTeams; ++t) M = fmaxf(M, mml[((t * C::kSplit + cm) * GW + k) * 2]);
         float L = 0.f, O = 0.f;
-        for (int w = 0; w < NCW; ++w) {
-            const float *row = fsm + ((size_t)w * g + n) * (D + 2);
-            const float f = (row[0] == -INFINITY) ? 0.f : exp2f(row[0] - M);
-            L += row[1] * f;
-            O += row[2 + d] * f;
+#pragma unroll
+        for (int t = 0; t < C::kTeams; ++t) {
+            const int r = (t * C::kSplit + cm) * GW + k;
+            const float mw = mml[r * 2];
+            const float f = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
+            L += mml[r * 2 + 1] * f;
+            O += macc[r * C::kMergeStride + d] * f;
         }
         const float o = O / L;
-        const size_t orow = (size_t)s * p.num_q_heads + (size_t)h * g + n;
         if (npart == 1) {
-            out[orow * D + d] = o;
+            out[(orow0 + col) * D + d] = o;
         } else {
-            const size_t r = orow * p.max_parts + part;
+            const size_t r = (orow0 + col) * p.max_parts + part;
             p.ws_o[r * D + d] = o;
             if (d == 0) {
                 p.ws_ml[r * 2 + 0] = M;

@@ -62,6 +62,11 @@ CASES = [
     ("f32_gqa16_d64", "f32", 16, 1, 64),
     ("f32_mha_d128", "f32", 4, 4, 128),
     ("f32_gqa8_d128", "f32", 16, 2, 128),
+    ("f32_gqa2_d128", "f32", 4, 2, 128),
+    ("f32_gqa3_d64", "f32", 6, 2, 64),
+    ("f32_gqa6_d128", "f32", 12, 2, 128),
+    ("f32_gqa12_d64", "f32", 12, 1, 64),
+    ("f32_gqa16_d128", "f32", 32, 2, 128),
 ]
 
 
