@@ -270,10 +270,7 @@ template <int D, bool kUnits>
 int launch_prefill_tc(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUtensorMap &tmv,
                       const pkv::PrefillParams &pp, dim3 grid, cudaStream_t st) {
     using C = pkv::TcCfg<D>;
-    // dynamic plus the kernels' static shared memory (the sequence ranking's counts)
-    static_assert(C::kSmem + 4 * (pkv::kRankMaxSeqs + 8) <= (int)kSmemLimit, "shared memory");
-    static_assert(C::kSmemUnits + 4 * (pkv::kRankMaxSeqs + 8) <= (int)kSmemLimit, "shared memory");
-    constexpr int smem = kUnits ? C::kSmemUnits : C::kSmem;
+    static_assert(C::kSmem <= (int)kSmemLimit, "shared memory");
     auto kern = kUnits ? pkv::prefill_tc_units_kernel<D> : pkv::prefill_tc_kernel<D>;
     static thread_local int configured_device = -1;
     int dev = 0;
@@ -285,11 +282,11 @@ int launch_prefill_tc(const CUtensorMap &tmq, const CUtensorMap &tmk, const CUte
         if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return PKV_ERR_CUDA;
         if (fa.numRegs * C::kThreads < 128 * C::kLowRegs + C::kTiles * 128 * C::kHighRegs)
             return PKV_ERR_UNSUPPORTED;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured_device = dev;
     }
-    kern<<<grid, C::kThreads, smem, st>>>(tmq, tmk, tmv, pp);
+    kern<<<grid, C::kThreads, C::kSmem, st>>>(tmq, tmk, tmv, pp);
     return check_launch();
 }
 

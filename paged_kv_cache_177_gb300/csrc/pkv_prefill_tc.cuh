@@ -77,10 +77,6 @@ struct TcCfg {
     static constexpr int kVOff = kKOff + kStages * kStage;
     static constexpr int kBarOff = kVOff + kStages * kStage;
     static constexpr int kSmem = kBarOff + 256 + 1024;     // + barriers, + 1024-byte alignment slack
-    // per-unit kernel: a third query-tile buffer past the barriers (1024-byte aligned for the swizzle)
-    static constexpr int kQ2Off = kBarOff + 1024;
-    static constexpr int kSmemUnits = kQ2Off + kQBytes + 1024;
-    __host__ __device__ static constexpr int q_off(int buf) { return buf < 2 ? kQOff + buf * kQBytes : kQ2Off; }
     static constexpr int kSoftmaxWarps = 4 * kTiles;
     static constexpr int kThreads = (4 + kSoftmaxWarps) * 32;  // warpgroup 0: TMA, MMA, 2 idle warps
     // register split (setmaxnreg): launched at kLaunchRegs each, warpgroup 0 gives
@@ -100,7 +96,7 @@ struct TcBars {
     uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
     uint64_t s_full[2], p_full[2], o_done[2];  // per query tile
     uint64_t drain;
-    uint64_t qf[3], qe[3];  // per-unit kernel: query-tile buffer loaded / read by its tile's last S
+    uint64_t q_empty;  // per-unit kernel: the pair's last S has read Q
     uint32_t tmem_base;
 };
 
@@ -532,10 +528,8 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
 // the CTA's set-up (tensor-memory allocation, barriers) is paid once, and the next pair's Q
 // and first K/V chunk load while the current pair finishes. The roles are those of
 // prefill_tc_kernel, each looping over the pairs; barrier phases run on across pairs (a
-// K/V ring position over all the CTA's chunks, per-tile S / P and O phase counts). Query
-// tiles rotate through three buffers, loaded by warp 2: while a pair runs on two of them the
-// next pair's first tile is already in the third, and its second tile loads as soon as the
-// current pair's first tile has issued its last S (a tile's last S commits its buffer's qe).
+// K/V ring position over all the CTA's chunks, per-tile S / P and O phase counts), and a
+// q_empty barrier lets the next pair's Q land only once the last S of the pair has read Q.
 template <int D>
 __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
     prefill_tc_units_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -590,10 +584,8 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
         prefetch_tensormap(&tmq);
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
-        for (int i = 0; i < 3; ++i) {
-            mbar_init(&b.qf[i], 1);
-            mbar_init(&b.qe[i], 1);
-        }
+        mbar_init(&b.q_full, 1);
+        mbar_init(&b.q_empty, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&b.k_full[i], 1);
             mbar_init(&b.k_empty[i], 1);
@@ -614,7 +606,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = b.tmem_base;
-    const uint32_t k_s = smem_u32(base + C::kKOff);
+    const uint32_t q_s = smem_u32(base + C::kQOff), k_s = smem_u32(base + C::kKOff);
     const uint32_t v_s = smem_u32(base + C::kVOff);
 
     if (warp < 4) {
@@ -624,10 +616,26 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
         if (lane == 0) {
             bool ok = true;
             const int32_t *table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-            int issued_k = 0, issued_v = 0;  // K / V chunks issued (all pairs)
+            int issued_k = 0, issued_v = 0, issued_q = 0;  // K / V chunks (all pairs) and Q tiles issued
             for (int it = 0; it < npairs && ok; ++it) {
-            int nc[C::kTiles];
-            const int nc_all = pair_chunks(it, nc);
+            int t0[C::kTiles], t_end[C::kTiles], nc[C::kTiles];
+            const int nc_all = pair_tiles(it, t0, t_end, nc);
+            // the previous pair's last S has read Q before this pair's Q lands there
+            if (it > 0 && !mbar_wait(&b.q_empty, (it - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            int qbytes = 0;
+#pragma unroll
+            for (int t = 0; t < C::kTiles; ++t) qbytes += nc[t] > 0 ? C::kHalves * 128 * g * tt : 0;
+            mbar_arrive_expect_tx(&b.q_full, qbytes);
+#pragma unroll
+            for (int t = 0; t < C::kTiles; ++t)
+                if (nc[t] > 0)
+                    for (int u = 0; u < C::kHalves; ++u)
+                        tma_load_4d(base + C::kQOff + t * C::kQBytes + u * C::kHalfRows, &tmq, 0, u, h * g,
+                                    q0 + t0[t], &b.q_full);
+            issued_q = it + 1;
             for (int j = 0; j < nc_all && ok; ++j) {
                 const int gj = issued_k;  // ring position over all the CTA's chunks
                 const int st = gj & 1;
@@ -685,44 +693,18 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
             // no copy may land after the CTA is gone: wait (bounded) for the last one of each stage
             for (int j = max(0, issued_k - 2); j < issued_k; ++j) mbar_wait(&b.k_full[j & 1], (j >> 1) & 1);
             for (int j = max(0, issued_v - 2); j < issued_v; ++j) mbar_wait(&b.v_full[j & 1], (j >> 1) & 1);
-        }
-    } else if (warp == 2) {
-        // ------------------------------ query tiles ------------------------------
-        // the CTA's non-empty tiles in order, tile number u in buffer u % 3
-        if (lane == 0) {
-            bool ok = true;
-            int u = 0;
-            for (int it = 0; it < npairs && ok; ++it) {
-                int t0[C::kTiles], t_end[C::kTiles], nc[C::kTiles];
-                pair_tiles(it, t0, t_end, nc);
-#pragma unroll
-                for (int t = 0; t < C::kTiles; ++t) {
-                    if (nc[t] == 0) continue;
-                    const int bq = u % 3;
-                    if (u >= 3 && !mbar_wait(&b.qe[bq], (u / 3 - 1) & 1)) {  // tile u - 3 has read it
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&b.qf[bq], C::kHalves * 128 * g * tt);
-                    for (int hf = 0; hf < C::kHalves; ++hf)
-                        tma_load_4d(base + C::q_off(bq) + hf * C::kHalfRows, &tmq, 0, hf, h * g, q0 + t0[t], &b.qf[bq]);
-                    ++u;
-                }
-            }
-            if (!ok) raise_error(PKV_DEVERR_TIMEOUT);
-            // no copy may land after the CTA is gone: wait (bounded) for the last ones
-            for (int v = max(0, u - 3); v < u; ++v) mbar_wait(&b.qf[v % 3], (v / 3) & 1);
+            if (issued_q > 0) mbar_wait(&b.q_full, (issued_q - 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(C::kRows, C::kKeys, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(C::kRows, D, false, true);
-            // S of tile t (query buffer bq) from the K chunk in ring position gj
-            auto issue_s = [&](int t, int bq, int gj) {
+            // S of tile t from the K chunk in ring position gj
+            auto issue_s = [&](int t, int gj) {
                 // (opaque bases: the descriptors are built at the issue, not hoisted and held in
                 // registers across the pair loop)
-                uint32_t qb = smem_u32(base + C::q_off(bq)), kb = k_s + (gj & 1) * C::kStage;
+                uint32_t qb = q_s + t * C::kQBytes, kb = k_s + (gj & 1) * C::kStage;
                 asm volatile("" : "+r"(qb), "+r"(kb));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {  // 16 head-dim elements per step
@@ -748,25 +730,20 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
             bool ok = true;
             int kv = 0;                // ring position of the pair's first chunk
             int cs[C::kTiles] = {};    // per tile: chunks of the earlier pairs (S / P phases)
-            int u = 0;                 // non-empty tiles so far (query buffer u % 3)
             for (int it = 0; it < npairs && ok; ++it) {
-                int nc[C::kTiles], bq[C::kTiles];
+                int nc[C::kTiles];
                 const int nc_all = pair_chunks(it, nc);
-                ok = mbar_wait(&b.k_full[kv & 1], (kv >> 1) & 1);
-#pragma unroll
-                for (int t = 0; t < C::kTiles; ++t) {
-                    bq[t] = u % 3;
-                    if (nc[t] == 0 || !ok) continue;
-                    ok = mbar_wait(&b.qf[bq[t]], (u / 3) & 1);
-                    ++u;
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(t, bq[t], kv);
-                    umma_commit(&b.s_full[t]);
-                    if (nc[t] == 1) umma_commit(&b.qe[bq[t]]);  // the tile's last S
-                }
+                ok = mbar_wait(&b.q_full, it & 1) && mbar_wait(&b.k_full[kv & 1], (kv >> 1) & 1);
                 if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int t = 0; t < C::kTiles; ++t)
+                    if (nc[t] > 0) {
+                        issue_s(t, kv);
+                        umma_commit(&b.s_full[t]);
+                    }
                 umma_commit(&b.k_empty[kv & 1]);
+                if (nc_all == 1) umma_commit(&b.q_empty);  // the pair's last S has been issued
                 for (int j = 0; ok && j < nc_all; ++j) {
                     const int gj = kv + j;
                     ok = mbar_wait(&b.v_full[gj & 1], (gj >> 1) & 1);
@@ -779,9 +756,8 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                         tc_fence_after();
                         issue_pv(t, j, gj);
                         if (j + 1 < nc[t]) {
-                            issue_s(t, bq[t], gj + 1);
+                            issue_s(t, gj + 1);
                             umma_commit(&b.s_full[t]);
-                            if (j + 2 == nc[t]) umma_commit(&b.qe[bq[t]]);  // the tile's last S
                         } else {
                             umma_commit(&b.o_done[t]);
                         }
@@ -789,6 +765,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                     if (!ok) break;
                     umma_commit(&b.v_empty[gj & 1]);
                     if (j + 1 < nc_all) umma_commit(&b.k_empty[(gj + 1) & 1]);
+                    if (j + 2 == nc_all) umma_commit(&b.q_empty);  // the pair's last S has been issued
                 }
 #pragma unroll
                 for (int t = 0; t < C::kTiles; ++t) cs[t] += nc[t];
