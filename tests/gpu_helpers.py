@@ -77,14 +77,23 @@ def path_switching_calls():
     2. a 13B-class batch of 64, automatic: the persistent kernel, whose
        arrival counters must read zero although call 1 wrote partials;
     3. fixed 128-token partitions on a GQA batch with edge lengths;
-    4. a larger GQA batch, automatic: the persistent kernel again."""
+    4. a larger GQA batch, automatic: the persistent kernel again;
+    5. a GQA batch with fp32 caches split into partitions (the staged fp32
+       kernel writes its partial states after the counter header too)."""
     return [
         ("grid split", W.make_workload("mha13b", lengths_list=(600, 1500, 2048, 513, 1024, 77, 1800, 900),
                                        seed=301), 0, False),
         ("persistent", W.make_workload("mha13b", seed=302), 0, True),
         ("fixed partitions", W.make_workload("gqa8b", lengths_list=EDGE_LENGTHS, seed=303), 128, False),
         ("persistent, larger batch", W.make_workload("gqa8b", num_seqs=160, len_hi=1500, seed=304), 0, True),
+        ("fp32 grid split", W.make_workload("gqa8b", lengths_list=(600, 1500, 2048, 513, 77, 1024), dtype="f32",
+                                            seed=305), 0, False),
     ]
+
+
+def torch_dtype(spec):
+    """The cache element type of a workload spec."""
+    return torch.bfloat16 if spec.dtype == "bf16" else torch.float32
 
 
 def prepared(case):

@@ -283,11 +283,11 @@ def test_persistent_path_leaves_counters_zero_and_repeats_bit_identically():
 
 def test_one_workspace_serves_every_decode_path_in_turn():
     """One workspace, zero-filled once and sized for the largest call, serves
-    a split grid call, a persistent call, a fixed-partition call and a
-    persistent call on a larger batch, in that order (a serving loop whose
-    batch crosses the persistent threshold): every output matches the oracle
-    on every sequence and head, and the counter header is zero after each
-    call."""
+    a split grid call, a persistent call, a fixed-partition call, a
+    persistent call on a larger batch and a split fp32 call, in that order (a
+    serving loop whose batch crosses the persistent threshold): every output
+    matches the oracle on every sequence and head, and the counter header is
+    zero after each call."""
     b = H.lib()
     cases = H.path_switching_calls()
     need = max(b.workspace_bytes(wc.spec.num_seqs, wc.spec.num_q_heads, wc.spec.num_kv_heads, wc.spec.head_dim,
@@ -296,7 +296,7 @@ def test_one_workspace_serves_every_decode_path_in_turn():
     for case in cases + cases[:2]:
         label, wc, pt, persistent = case
         sp, lay = wc.spec, wc.layout
-        assert b.decode_persistent(sp.num_seqs, sp.num_kv_heads, pt, torch.bfloat16) == persistent, label
+        assert b.decode_persistent(sp.num_seqs, sp.num_kv_heads, pt, H.torch_dtype(sp)) == persistent, label
         assert persistent or b.decode_launches(sp.num_seqs, sp.num_kv_heads, lay.max_context_len, pt) == 2, label
         w, ref = H.prepared(case)
         out = torch.full_like(w.q, float("nan"))
@@ -304,7 +304,7 @@ def test_one_workspace_serves_every_decode_path_in_turn():
                                  max_context_len=lay.max_context_len, partition_tokens=pt, workspace=ws)
         torch.cuda.synchronize()
         assert int(ws[: b.DECODE_COUNTER_BYTES].count_nonzero()) == 0, label
-        H.assert_close(out, ref, "bf16", f"reused workspace, {label}")
+        H.assert_close(out, ref, sp.dtype, f"reused workspace, {label}")
         del w
 
 

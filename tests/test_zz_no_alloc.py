@@ -54,7 +54,7 @@ def _run(fn, case):
     sp = wc.spec
     need = b.workspace_bytes(sp.num_seqs, sp.num_q_heads, sp.num_kv_heads, sp.head_dim, wc.layout.max_context_len, pt)
     assert 0 < need <= STATIC_BYTES, label           # the call really uses the scratch
-    assert b.decode_persistent(sp.num_seqs, sp.num_kv_heads, pt, torch.bfloat16) == persistent, label
+    assert b.decode_persistent(sp.num_seqs, sp.num_kv_heads, pt, H.torch_dtype(sp)) == persistent, label
     w, ref = H.prepared(case)
     out = torch.full_like(w.q, float("nan"))
     assert _call_static(fn, out, w, pt) == 0, label
@@ -66,8 +66,8 @@ def _run(fn, case):
 
 def test_static_workspace_matches_the_oracle_on_calls_that_switch_paths():
     """Split grid, persistent, fixed partitions, persistent on a larger batch,
-    then split grid and persistent again -- six calls in a row on the one
-    array."""
+    split fp32, then split grid and persistent again -- seven calls in a row on
+    the one array."""
     torch.cuda.set_device(0)
     fn = _entry()
     cases = H.path_switching_calls()
