@@ -1417,7 +1417,6 @@ struct PrefillParams {
 
 template <int D, int GMAX, int NSTAGE, int NCW>
 struct F32Cfg {
-    static constexpr int kSubBytes = kBlock * 128;               // 2 KiB: 16 rows of 32 fp32
     static constexpr int kTile = kBlock * D * 4;                 // one (block, head) tile of K or V
     static constexpr int kStage = 2 * kTile;                     // K tile + V tile
     static constexpr int kThreads = (NCW + 1) * 32;
@@ -1439,14 +1438,16 @@ struct F32Cfg {
 };
 
 // One warp's online-softmax state for g <= GMAX query heads of a kv head (all of the
-// group's, or one warp's share of them), over fp32 K/V tiles staged as F32Cfg lays them out. Scores: lane (quarter h4 = lane / 8,
-// token t8 = lane % 8) dots its quarter of the head dimension for tokens t8 and t8 + 8
-// with every head's query (packed fp32 pairs), then two shuffles add the quarters. The
-// softmax weights go through the warp's shared-memory slot so that P V can take four
-// tokens' weights of a head in one broadcast load; lane l accumulates head-dim elements
-// kDims l .. kDims l + kDims - 1 of every head.
+// group's, or one warp's share of them), over fp32 K/V tiles staged as F32Cfg lays them
+// out. Scores: lane (quarter h4 = lane / 8, token t8 = lane % 8) dots its quarter of the
+// head dimension for tokens t8 and t8 + 8 with every head's query (packed fp32 pairs),
+// then two shuffles add the quarters. The softmax weights go through the warp's
+// shared-memory slot so that P V can take four tokens' weights of a head in one
+// broadcast load; lane l accumulates head-dim elements kDims l .. kDims l + kDims - 1 of
+// every head.
 template <int D, int GMAX>
 struct WarpAttnF32 {
+    static constexpr int kSubBytes = kBlock * 128;  // 2 KiB: 16 rows of 32 fp32
     static constexpr int kQC = D / 16;        // 16-byte chunks in a quarter row
     static constexpr int kDims = D / 32;      // output elements per lane (4 or 2)
     static constexpr int kQuarterBytes = D + 16;
@@ -1481,7 +1482,7 @@ struct WarpAttnF32 {
         const int h4 = lane >> 3, t8 = lane & 7;
         constexpr int kLaneBytes = kDims * 4;
         const int ci_v = (lane * kLaneBytes) >> 4;
-        const uint32_t vbase = sv + (ci_v >> 3) * (kBlock * 128) + ((lane * kLaneBytes) & 15);
+        const uint32_t vbase = sv + (ci_v >> 3) * kSubBytes + ((lane * kLaneBytes) & 15);
         const int cv = ci_v & 7;
 #pragma unroll
         for (int hg = 0; hg < GMAX; hg += kHG) {
@@ -1493,7 +1494,7 @@ struct WarpAttnF32 {
             for (int j = 0; j < kQC; ++j) {
                 const int ci = h4 * kQC + j;  // 16-byte chunk of the row
                 const int u = ci >> 3, c = ci & 7;
-                const uint32_t at = sk + u * (kBlock * 128) + ((c ^ t8) << 4);  // rows t8, t8 + 8 share the swizzle
+                const uint32_t at = sk + u * kSubBytes + ((c ^ t8) << 4);  // rows t8, t8 + 8 share the swizzle
                 uint32_t x[4], y[4];
                 ld_shared_v4(at + t8 * 128, x);
                 ld_shared_v4(at + (t8 + 8) * 128, y);
