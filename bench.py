@@ -755,7 +755,7 @@ def run_ours(args, rank, world, local, dist):
             (parity is None or parity["within_bound"]) and
             all(c["parity"]["within_bound"] for c in configs.values() if isinstance(c, dict)))
         # the rows beyond the decode step: shared-prefix decode and prefill, each timed and checked
-        next_rows = {"shared_prefix": shared_prefix_measure(args.config_steps // 10, dev, B, evict),
+        next_rows = {"shared_prefix": shared_prefix_measure(max(args.config_steps // 10, 3), dev, B, evict),
                      "prefill": {name: prefill_measure(name, 30, dev, B, evict, oracle_seqs=2)
                                  for name in W.PREFILL_SPECS}}
     srt = sorted(step_ms)
@@ -952,7 +952,8 @@ def run_op(args, rank, world, local, dist):
 
 def graph_time(fn, n, dev, evict):
     """Median device time of fn, captured once as a CUDA graph and replayed
-    after an L2 eviction each time."""
+    after an L2 eviction each time (at least once)."""
+    n = max(n, 1)
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(side):
