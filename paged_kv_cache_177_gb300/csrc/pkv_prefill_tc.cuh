@@ -49,7 +49,12 @@
 // prefill_tc_units_kernel runs the same roles with one CTA per (sequence, kv
 // head) looping over all its pairs: for batches of whole prompts with many such
 // units, where each pair is short and a CTA's set-up would otherwise be paid
-// once per pair.
+// once per pair. It gives the remainder only in tiles holding rows that see at
+// most kPrefillSplitPositions keys (the rows the remainder is for; on every tile it
+// cost about 13% of the kernel's time on whole prompts: a second P V and the
+// remainders' softmax work on each first chunk), its first chunk's softmax compiled
+// apart from the others'. The one-pair kernel keeps the remainder on every tile's first chunk:
+// there the same restriction compiled into slower code.
 //
 // Every wait is bounded; on a timeout the CTA records PKV_DEVERR_TIMEOUT,
 // waits (bounded) for its in-flight copies and MMAs, frees its tensor memory
@@ -105,7 +110,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+template <bool B>
+struct BoolConst {  // a compile-time flag passed to a generic lambda
+    static constexpr bool value = B;
+};
+
 constexpr int kRankMaxSeqs = 128;  // batches up to this size can be issued longest-first
+
+// Query rows at positions below this see at most this many keys. In the per-unit kernel
+// only the tiles holding such rows give their first chunk's weights to P V as bf16 plus
+// the rounding remainder.
+constexpr int kPrefillSplitPositions = 64;
 
 // The sequence a CTA with sequence rank z works on: in batches of up to
 // kRankMaxSeqs sequences, the z-th by context length (longest first, ties by
@@ -714,8 +729,9 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                 }
             };
             // O of tile t += P V, chunk j of the pair from the V chunk in ring position gj
-            auto issue_pv = [&](int t, int j, int gj) {
-                const bool split = j == 0;  // the first chunk's weights carry their rounding remainder
+            auto issue_pv = [&](int t, int j, int gj, bool split_tile) {
+                // the first chunk's weights carry their rounding remainder in tiles with rows that see few keys
+                const bool split = j == 0 && split_tile;
                 uint32_t vb = v_s + (gj & 1) * C::kStage;
                 asm volatile("" : "+r"(vb));
 #pragma unroll
@@ -733,6 +749,10 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
             for (int it = 0; it < npairs && ok; ++it) {
                 int nc[C::kTiles];
                 const int nc_all = pair_chunks(it, nc);
+                int split_tiles = 0;  // tiles whose first chunk is split, one bit each
+#pragma unroll
+                for (int t = 0; t < C::kTiles; ++t)
+                    split_tiles |= (first_pos + ((pair_hi - it) * C::kTiles + t) * tt < kPrefillSplitPositions) << t;
                 ok = mbar_wait(&b.q_full, it & 1) && mbar_wait(&b.k_full[kv & 1], (kv >> 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
@@ -754,7 +774,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
                         if (j >= nc[t]) continue;
                         if (!(ok = mbar_wait(&b.p_full[t], (cs[t] + j) & 1))) break;
                         tc_fence_after();
-                        issue_pv(t, j, gj);
+                        issue_pv(t, j, gj, (split_tiles >> t) & 1);
                         if (j + 1 < nc[t]) {
                             issue_s(t, gj + 1);
                             umma_commit(&b.s_full[t]);
@@ -828,6 +848,7 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
         const bool row_ok = row < rows;
         pos = row_ok ? first_pos + tok0 + row / g : -1;
         const int tile_first = first_pos + tok0;  // the smallest query position of the tile
+        const bool split_tile = tile_first < kPrefillSplitPositions;  // its rows include some that see few keys
         float m = -INFINITY, l = 0.f;
         for (int j = 0; j < ncs; ++j) {
             if (!(ok = warp_wait(&b.s_full[t], (cs + j) & 1))) break;
@@ -877,39 +898,41 @@ __global__ void __launch_bounds__(TcCfg<D>::kThreads, 1)
             // keys 32 q + 2 i, + 1 at column 32 q + i, their rounding remainders at + 16.
             // The row sum takes the unrounded weights: the first chunk's P (hi + lo) matches
             // them to 2^-16, later chunks' rounding errors average out over the keys.
-            const bool split = j == 0;
-            const uint64_t sl2 = pack_f2(sl, sl), nms2 = pack_f2(-ms, -ms);
-            uint64_t rss[4];  // independent partial sums, two lanes each
+            // (compiled twice: the first chunk's instance with the remainders, the others' without,
+            // so the common chunk's code carries none of the split's instructions or registers)
+            auto write_p = [&](auto split_c) -> float {
+                constexpr bool split = decltype(split_c)::value;
+                const uint64_t sl2 = pack_f2(sl, sl), nms2 = pack_f2(-ms, -ms);
+                uint64_t rss[4];  // independent partial sums, two lanes each
 #pragma unroll
-            for (int i = 0; i < 4; ++i) rss[i] = pack_f2(0.f, 0.f);
+                for (int i = 0; i < 4; ++i) rss[i] = pack_f2(0.f, 0.f);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t hi[16], lo[16];
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t hi[16], lo[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float a0, a1;
-                    unpack_f2(fma_f2(pack_f2(x[q][2 * i], x[q][2 * i + 1]), sl2, nms2), a0, a1);
-                    const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
-                    rss[i & 3] = add_f2(rss[i & 3], pack_f2(e0, e1));
-                    const __nv_bfloat162 ph = __floats2bfloat162_rn(e0, e1);
-                    hi[i] = *reinterpret_cast<const uint32_t *>(&ph);
-                    if (split) {
-                        const float2 fh = __bfloat1622float2(ph);
-                        const __nv_bfloat162 pl = __floats2bfloat162_rn(e0 - fh.x, e1 - fh.y);
-                        lo[i] = *reinterpret_cast<const uint32_t *>(&pl);
+                    for (int i = 0; i < 16; ++i) {
+                        float a0, a1;
+                        unpack_f2(fma_f2(pack_f2(x[q][2 * i], x[q][2 * i + 1]), sl2, nms2), a0, a1);
+                        const float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+                        rss[i & 3] = add_f2(rss[i & 3], pack_f2(e0, e1));
+                        const __nv_bfloat162 ph = __floats2bfloat162_rn(e0, e1);
+                        hi[i] = *reinterpret_cast<const uint32_t *>(&ph);
+                        if constexpr (split) {
+                            const float2 fh = __bfloat1622float2(ph);
+                            const __nv_bfloat162 pl = __floats2bfloat162_rn(e0 - fh.x, e1 - fh.y);
+                            lo[i] = *reinterpret_cast<const uint32_t *>(&pl);
+                        }
                     }
+                    tmem_st16(cols + q * 32, hi);
+                    if constexpr (split) tmem_st16(cols + q * 32 + 16, lo);
                 }
-                tmem_st16(cols + q * 32, hi);
-                if (split) tmem_st16(cols + q * 32 + 16, lo);
-            }
-            tmem_wait_st();
-            float rs;
-            {
+                tmem_wait_st();
                 float r[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) unpack_f2(rss[i], r[2 * i], r[2 * i + 1]);
-                rs = ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
-            }
+                return ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
+            };
+            const float rs = j == 0 && split_tile ? write_p(BoolConst<true>{}) : write_p(BoolConst<false>{});
             l = l * alpha + rs;
             tc_fence_before();
             __syncwarp();

@@ -169,8 +169,13 @@ def test_cta_order_does_not_change_the_result(num_seqs):
     longer than the new tokens, else one sequence at a time in decreasing order
     of context length (ranked inside the kernel for batches of up to 128 sequences,
     in index order beyond). A larger host bound on the context length selects
-    the second order for the same inputs: the outputs are bit-identical, and
-    match the oracle. Lengths repeat, so the ranking meets ties."""
+    the second order for the same inputs: both outputs match the oracle, and
+    where the same kernel runs both orders (24 sequences x 8 kv heads, too few
+    units for the per-unit kernel) they are bit-identical. With 130 sequences
+    the first order runs the per-unit kernel, which splits the first chunk's
+    weights only in tiles holding rows that see at most 64 keys, so other
+    tiles' first-chunk weights round differently there. Lengths repeat, so the
+    ranking meets ties."""
     rng = np.random.default_rng(num_seqs)
     new = tuple(int(x) for x in rng.choice([1, 7, 64, 130, 300] if num_seqs < 100 else [1, 7, 40, 150], num_seqs))
     prior = tuple(int(x) for x in rng.choice([0, 5, 100], num_seqs))
@@ -188,5 +193,7 @@ def test_cta_order_does_not_change_the_result(num_seqs):
                                   wg.query_start, wg.scale, max_query_len=w.max_query_len, max_context_len=bound)
         torch.cuda.synchronize()
         outs.append(out)
-    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
-    H.assert_close(outs[0], ref, "bf16", f"{num_seqs} sequences")
+    for o, order in zip(outs, ("pair index slowest", "one sequence at a time")):
+        H.assert_close(o, ref, "bf16", f"{num_seqs} sequences, {order}")
+    if w.spec.num_seqs * w.spec.num_kv_heads < 4 * torch.cuda.get_device_properties(0).multi_processor_count:
+        assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
