@@ -190,6 +190,11 @@ def kernel_source_sha256(kernel: str) -> str:
     return h.hexdigest()
 
 
+def f32_kernel_name(sp) -> str:
+    """The fp32 decode kernel for a workload's group size (tensor cores past four heads)."""
+    return "decode_f32_tc_kernel" if sp.num_q_heads // sp.num_kv_heads > 4 else "decode_f32_staged_kernel"
+
+
 def profiled_traffic(workload: str, kernel: str):
     """(DRAM bytes per launch, summary file) from the committed ncu summary, or
     (None, reason) when there is none or the kernel changed since it was taken."""
@@ -464,7 +469,7 @@ def config_summary(name: str, args, dev, B, evict) -> dict:
     gbs, secs, nseq, passes, sb = oracle_sample(lay, host, args.config_cpu_seconds)
     parity = full_parity(lay, host, out, sp.dtype, out32)
     kernel = ("decode_bf16_persistent_kernel" if persistent else
-              ("decode_bf16_kernel" if sp.dtype == "bf16" else "decode_f32_staged_kernel") +
+              ("decode_bf16_kernel" if sp.dtype == "bf16" else f32_kernel_name(sp)) +
               (" + lse_reduce_kernel" if launches == 2 else ""))
     res = {
         "workload": describe(sp),
@@ -760,7 +765,7 @@ def run_ours(args, rank, world, local, dist):
                                  for name in W.PREFILL_SPECS}}
     srt = sorted(step_ms)
     roof_kernel = ("decode_bf16_persistent_kernel" if persistent else
-                   "decode_bf16_kernel" if sp.dtype == "bf16" else "decode_f32_staged_kernel")
+                   "decode_bf16_kernel" if sp.dtype == "bf16" else f32_kernel_name(sp))
     # the captures were taken on the workloads' default launch configuration
     traffic, traffic_src = profiled_traffic(sp.name if args.partition_tokens is None and args.dtype is None else "",
                                             roof_kernel)

@@ -217,6 +217,39 @@ int launch_f32_staged(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv:
     return check_launch();
 }
 
+// fp32 caches with more than four query heads per kv head: the tensor-core step, two
+// consumer warps with two of the four stages each (at d = 128 a CTA then fits three to an
+// SM; four consumer warps of one stage each measured 7% slower on the 32K-128K-token batch).
+#ifndef PKV_F32_TC
+#define PKV_F32_TC 1
+#endif
+#ifndef PKV_F32_TC_NCW
+#define PKV_F32_TC_NCW 2
+#endif
+#ifndef PKV_F32_TC_STAGES
+#define PKV_F32_TC_STAGES 4
+#endif
+constexpr bool kF32Tc = PKV_F32_TC != 0;
+
+template <int D, int GMAX>
+int launch_f32_tc(const CUtensorMap &tmk, const CUtensorMap &tmv, const pkv::DecodeParams &p, dim3 grid,
+                  cudaStream_t st, bool pdl) {
+    using C = pkv::F32TcCfg<D, GMAX, PKV_F32_TC_STAGES, PKV_F32_TC_NCW>;
+    static_assert(C::kSmem <= (int)kSmemLimit, "shared memory");
+    auto kern = pkv::decode_f32_tc_kernel<D, GMAX, PKV_F32_TC_STAGES, PKV_F32_TC_NCW>;
+    static thread_local int configured_device = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (configured_device != dev) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured_device = dev;
+    }
+    if (pdl) return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmem, st, tmk, tmv, p);
+    kern<<<grid, C::kThreads, C::kSmem, st>>>(tmk, tmv, p);
+    return check_launch();
+}
+
 // fp32 caches: the tensor maps of both caches, then the instance for the group size.
 template <int D>
 int launch_f32(const pkv::DecodeParams &p, dim3 grid, cudaStream_t st, bool pdl) {
@@ -228,6 +261,7 @@ int launch_f32(const pkv::DecodeParams &p, dim3 grid, cudaStream_t st, bool pdl)
     if (g == 1) return launch_f32_staged<D, 1>(tmk, tmv, p, grid, st, pdl);
     if (g == 2) return launch_f32_staged<D, 2>(tmk, tmv, p, grid, st, pdl);
     if (g <= 4) return launch_f32_staged<D, 4>(tmk, tmv, p, grid, st, pdl);
+    if (kF32Tc) return g <= 8 ? launch_f32_tc<D, 8>(tmk, tmv, p, grid, st, pdl) : launch_f32_tc<D, 16>(tmk, tmv, p, grid, st, pdl);
     if (g <= 8) return launch_f32_staged<D, 8>(tmk, tmv, p, grid, st, pdl);
     return launch_f32_staged<D, 16>(tmk, tmv, p, grid, st, pdl);
 }

@@ -1736,6 +1736,342 @@ __global__ void __launch_bounds__((NCW + 1) * 32, GMAX >= 16 ? 1 : (GMAX >= 8 ? 
 }
 
 // =====================================================================================
+// K1 (fp32, staged, tensor cores): the staged kernel's decomposition for groups of 5..16
+// query heads, with the per-block products on the tensor cores in tf32 split three ways.
+// An fp32 value x is hi + lo: hi = x rounded to tf32 (a 10-bit significand), lo = x - hi
+// exactly; the tensor core keeps lo to tf32 as well, so lo's dropped bits are below 2^-21
+// of x. A product a b is taken as ah bh + ah bl + al bh (three m16n8k8 MMAs with fp32
+// accumulation); the dropped al bl is below 2^-20 of |a b|.
+// =====================================================================================
+__device__ __forceinline__ void tf32_split(float x, uint32_t &hi, uint32_t &lo) {
+    uint32_t h;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(x));
+    hi = h;
+    lo = __float_as_uint(x - __uint_as_float(h));
+}
+
+// D = A(16x8, row) * B(8x8, col) + D, tf32 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_tf32_1688(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d += a b with a and b split as above
+__device__ __forceinline__ void mma_tf32x3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                           uint32_t bh0, uint32_t bh1, uint32_t bl0, uint32_t bl1) {
+    mma_tf32_1688(d, al, bh0, bh1);
+    mma_tf32_1688(d, ah, bl0, bl1);
+    mma_tf32_1688(d, ah, bh0, bh1);
+}
+
+// One warp's online-softmax state for the GMAX (8 or 16) query-head columns of a kv head
+// (columns past the group are zero queries, never read back), over fp32 K/V tiles staged as
+// F32Cfg lays them out. Per block: S^T (16 tokens x 8 heads per n-tile) = K Q^T, K
+// fragments by ldmatrix from the swizzled tile (a 32-bit element is a pair of b16), Q^T
+// fragments split once per CTA into shared memory; the softmax on the S^T fragments;
+// the weights through the warp's shared-memory slot into P^T fragments; then
+// O^T (D x 8 per n-tile) += V^T P^T with V^T fragments read element by element.
+template <int D, int GMAX>
+struct WarpAttnTF32 {
+    static constexpr int kNT = GMAX / 8;          // n-tiles of 8 query heads
+    static constexpr int kKS = D / 8;             // k-steps of S^T = K Q^T
+    static constexpr int kMT = D / 16;            // m-tiles of O^T
+    static constexpr int kSubBytes = kBlock * 128;
+    static constexpr int kHeadStride = 20;        // floats per head row of the weight slot (banks spread)
+    static constexpr int kQBytes = kNT * kKS * 32 * 16;          // split Q^T fragments, per lane 16 bytes
+    static constexpr int kPBytes = kNT * 8 * kHeadStride * 4;    // one warp's weights of a block
+    float m[kNT][2], l[kNT][2];   // columns nt 8 + 2 t and + 1 (t = lane % 4); l over this lane's tokens
+    float acc[kNT][kMT][4];       // O^T fragments: rows (dims) 16 mi + lane / 4 (+ 8), columns 2 t (+ 1)
+    uint32_t q_s, p_s;
+
+    // All threads of the CTA: the group's q (g heads at qg, D floats each) as split B
+    // fragments of S^T = K Q^T: entry (nt, ks, lane) holds hi and lo of q[head][8 ks + t]
+    // and q[head][8 ks + t + 4], head = 8 nt + lane / 4, t = lane % 4 (zero past the group).
+    static __device__ __forceinline__ void stage_q(uint8_t *dst, const float *qg, int g, int tid, int nthreads) {
+        for (int i = tid; i < kNT * kKS * 32; i += nthreads) {
+            const int ln = i & 31, ks = (i >> 5) % kKS, nt = i / (32 * kKS);
+            const int head = nt * 8 + (ln >> 2), dim = 8 * ks + (ln & 3);
+            const float b0 = head < g ? __ldg(qg + (size_t)head * D + dim) : 0.f;
+            const float b1 = head < g ? __ldg(qg + (size_t)head * D + dim + 4) : 0.f;
+            uint32_t h0, l0, h1, l1;
+            tf32_split(b0, h0, l0);
+            tf32_split(b1, h1, l1);
+            *reinterpret_cast<uint4 *>(dst + (size_t)i * 16) = make_uint4(h0, h1, l0, l1);
+        }
+    }
+
+    __device__ __forceinline__ void init(uint32_t q_smem, uint32_t p_smem) {
+        q_s = q_smem;
+        p_s = p_smem;
+    }
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                m[nt][hh] = -INFINITY;
+                l[nt][hh] = 0.f;
+            }
+#pragma unroll
+            for (int mi = 0; mi < kMT; ++mi)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[nt][mi][e] = 0.f;
+        }
+    }
+
+    // Rows below `lo` of the staged tiles are not tokens of the sequence (zero-filled by TMA).
+    __device__ __forceinline__ void block(uint32_t sk, uint32_t sv, int lo, float scale_log2, int lane) {
+        const int gq = lane >> 2, t = lane & 3;
+        // S^T = K Q^T
+        float sacc[kNT][4];
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+        // ldmatrix rows: lanes 8 m .. 8 m + 7 address matrix m = (token rows 8 (m & 1) .., 16-byte
+        // chunk m >> 1 of the k-step's two)
+        const int mrow = ((lane >> 3) & 1) * 8 + (lane & 7), mhalf = lane >> 4;
+#pragma unroll
+        for (int ks = 0; ks < kKS; ++ks) {
+            const int ch = 2 * (ks & 3) + mhalf;
+            uint32_t a[4], ah[4], al[4];
+            ldsm_x4(sk + (ks >> 2) * kSubBytes + mrow * 128 + ((ch ^ (mrow & 7)) << 4), a);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tf32_split(__uint_as_float(a[i]), ah[i], al[i]);
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) {
+                uint32_t qb[4];
+                ld_shared_v4(q_s + ((nt * kKS + ks) * 32 + lane) * 16, qb);
+                mma_tf32x3(sacc[nt], ah, al, qb[0], qb[1], qb[2], qb[3]);
+            }
+        }
+        // online softmax per column; lane holds tokens gq, gq + 8 of columns 2 t, 2 t + 1
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+            const float x00 = gq >= lo ? sacc[nt][0] * scale_log2 : -INFINITY;
+            const float x01 = gq >= lo ? sacc[nt][1] * scale_log2 : -INFINITY;
+            const float x10 = gq + 8 >= lo ? sacc[nt][2] * scale_log2 : -INFINITY;
+            const float x11 = gq + 8 >= lo ? sacc[nt][3] * scale_log2 : -INFINITY;
+            float mx0 = fmaxf(x00, x10), mx1 = fmaxf(x01, x11);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);  // finite: a block has a token
+            const float al0 = ex2_approx(m[nt][0] - mn0), al1 = ex2_approx(m[nt][1] - mn1);
+            m[nt][0] = mn0;
+            m[nt][1] = mn1;
+            const float p00 = ex2_approx(x00 - mn0), p10 = ex2_approx(x10 - mn0);
+            const float p01 = ex2_approx(x01 - mn1), p11 = ex2_approx(x11 - mn1);
+            l[nt][0] = l[nt][0] * al0 + (p00 + p10);
+            l[nt][1] = l[nt][1] * al1 + (p01 + p11);
+#pragma unroll
+            for (int mi = 0; mi < kMT; ++mi) {
+                acc[nt][mi][0] *= al0;
+                acc[nt][mi][2] *= al0;
+                acc[nt][mi][1] *= al1;
+                acc[nt][mi][3] *= al1;
+            }
+            // weights into the slot as [column][token]
+            const uint32_t ps = p_s + nt * 8 * kHeadStride * 4;
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(ps + ((2 * t) * kHeadStride + gq) * 4), "f"(p00) : "memory");
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(ps + ((2 * t + 1) * kHeadStride + gq) * 4), "f"(p01)
+                         : "memory");
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(ps + ((2 * t) * kHeadStride + gq + 8) * 4), "f"(p10)
+                         : "memory");
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(ps + ((2 * t + 1) * kHeadStride + gq + 8) * 4), "f"(p11)
+                         : "memory");
+        }
+        __syncwarp();
+        // O^T += V^T P^T, 8 tokens per k-step
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            uint32_t bh[kNT][2], bl[kNT][2];  // P^T fragments: tokens 8 kk + t (+ 4), column gq
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) {
+                const uint32_t ps = p_s + nt * 8 * kHeadStride * 4 + (gq * kHeadStride + 8 * kk + t) * 4;
+                float w0, w1;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(w0) : "r"(ps) : "memory");
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(w1) : "r"(ps + 16) : "memory");
+                tf32_split(w0, bh[nt][0], bl[nt][0]);
+                tf32_split(w1, bh[nt][1], bl[nt][1]);
+            }
+            const int t0 = 8 * kk + t, t1 = t0 + 4;
+#pragma unroll
+            for (int mi = 0; mi < kMT; ++mi) {
+                // V^T fragment: rows (dims) 16 mi + gq (+ 8), columns (tokens) t0, t1
+                const int d0 = 16 * mi + gq, d1 = d0 + 8;
+                const uint32_t a0 = sv + (d0 >> 5) * kSubBytes + t0 * 128 + ((((d0 & 31) >> 2) ^ (t0 & 7)) << 4) + (d0 & 3) * 4;
+                const uint32_t a1 = sv + (d1 >> 5) * kSubBytes + t0 * 128 + ((((d1 & 31) >> 2) ^ (t0 & 7)) << 4) + (d1 & 3) * 4;
+                const uint32_t a2 = sv + (d0 >> 5) * kSubBytes + t1 * 128 + ((((d0 & 31) >> 2) ^ (t1 & 7)) << 4) + (d0 & 3) * 4;
+                const uint32_t a3 = sv + (d1 >> 5) * kSubBytes + t1 * 128 + ((((d1 & 31) >> 2) ^ (t1 & 7)) << 4) + (d1 & 3) * 4;
+                float v[4];
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[0]) : "r"(a0));
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[1]) : "r"(a1));
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[2]) : "r"(a2));
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v[3]) : "r"(a3));
+                uint32_t ah[4], al[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) tf32_split(v[i], ah[i], al[i]);
+#pragma unroll
+                for (int nt = 0; nt < kNT; ++nt)
+                    mma_tf32x3(acc[nt][mi], ah, al, bh[nt][0], bh[nt][1], bl[nt][0], bl[nt][1]);
+            }
+        }
+        __syncwarp();  // the weights' slot is rewritten by the next block
+    }
+
+    __device__ __forceinline__ void reduce_l() {
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) l[nt][hh] += __shfl_xor_sync(0xffffffffu, l[nt][hh], o);
+    }
+
+    // Rows (columns of the group) 0 .. GMAX - 1 of the merge buffer.
+    __device__ __forceinline__ void store_merge(float *ml, float *acc_rows, int stride, int lane) const {
+        const int gq = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int col = nt * 8 + 2 * t + hh;
+                if (gq == 0) {
+                    ml[col * 2 + 0] = m[nt][hh];
+                    ml[col * 2 + 1] = l[nt][hh];
+                }
+#pragma unroll
+                for (int mi = 0; mi < kMT; ++mi) {
+                    acc_rows[col * stride + 16 * mi + gq] = acc[nt][mi][hh];
+                    acc_rows[col * stride + 16 * mi + gq + 8] = acc[nt][mi][2 + hh];
+                }
+            }
+    }
+};
+
+template <int D, int GMAX, int NSTAGE, int NCW>
+struct F32TcCfg {
+    using WA = WarpAttnTF32<D, GMAX>;
+    static constexpr int kTile = kBlock * D * 4;
+    static constexpr int kStage = 2 * kTile;
+    static constexpr int kThreads = (NCW + 1) * 32;
+    static constexpr int kMergeStride = D + 4;
+    static constexpr int kMergeBytes = NCW * GMAX * (2 + kMergeStride) * 4;
+    static constexpr int kBarOffset = NSTAGE * kStage;
+    static constexpr int kQOffset = kBarOffset + 2 * NSTAGE * 8;
+    static constexpr int kPOffset = kQOffset + WA::kQBytes;
+    static constexpr int kSmem = kPOffset + NCW * WA::kPBytes + 1024;  // + slack for 1 KiB alignment
+    static_assert(kMergeBytes <= kBarOffset, "merge buffer must fit in the stage ring");
+    static_assert(NSTAGE % NCW == 0, "each stage is always consumed by the same warp");
+    static_assert(kQOffset % 16 == 0 && WA::kPBytes % 16 == 0, "16-byte aligned areas");
+};
+
+template <int D, int GMAX, int NSTAGE, int NCW>
+__global__ void __launch_bounds__((NCW + 1) * 32)
+    decode_f32_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                         const DecodeParams p) {
+    using C = F32TcCfg<D, GMAX, NSTAGE, NCW>;
+    extern __shared__ uint8_t smem_raw[];
+
+    const int part = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = p.group;
+    const int len = seq_len(p, s, tid == 0 && part == 0 && h == 0);
+    const int nblk = (len + kBlock - 1) / kBlock;
+    const int npart = (nblk + p.part_blocks - 1) / p.part_blocks;
+    float *out = static_cast<float *>(p.out);
+
+    if (len == 0) {  // empty context: zero output rows
+        if (part == 0) {
+            float *o = out + ((size_t)s * p.num_q_heads + (size_t)h * g) * D;
+            for (int i = tid; i < g * D; i += C::kThreads) o[i] = 0.f;
+        }
+        return;
+    }
+    if (part >= npart) return;
+
+    const int b_begin = part * p.part_blocks;
+    const int nb = min(nblk - b_begin, p.part_blocks);
+    const int last_valid = len - (nblk - 1) * kBlock;  // tokens in the sequence's last block
+
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(base + C::kBarOffset);
+    uint64_t *empty = full + NSTAGE;
+    if (tid == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_fence_init();
+    }
+    const float *qg = static_cast<const float *>(p.q) + ((size_t)s * p.num_q_heads + (size_t)h * g) * D;
+    C::WA::stage_q(base + C::kQOffset, qg, g, tid, C::kThreads);
+    __syncthreads();
+
+    if (warp == NCW) {
+        grid_produce<C, NSTAGE>(tmk, tmv, p.block_tables + (size_t)s * p.max_blocks_per_seq, b_begin, nb, nblk - 1,
+                                last_valid, p.num_blocks, p.num_kv_heads, h, base, full, empty, lane);
+        return;
+    }
+    typename C::WA wa;
+    wa.init(smem_u32(base + C::kQOffset), smem_u32(base + C::kPOffset + warp * C::WA::kPBytes));
+    wa.reset();
+    const int last_in_range = (b_begin + nb - 1 == nblk - 1) ? nb - 1 : -1;
+    for (int j = warp; j < nb; j += NCW) {
+        const int st = j % NSTAGE;
+        if (!mbar_wait(&full[st], (j / NSTAGE) & 1)) {
+            raise_error(PKV_DEVERR_TIMEOUT);
+            break;
+        }
+        const uint32_t sk = smem_u32(base + st * C::kStage);
+        wa.block(sk, sk + C::kTile, j == last_in_range ? kBlock - last_valid : 0, p.scale_log2, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    wa.reduce_l();
+    named_barrier_sync(1, NCW * 32);  // every consumer is done with the stage ring
+    float *mml = reinterpret_cast<float *>(base);   // [NCW][GMAX][2]
+    float *macc = mml + NCW * GMAX * 2;              // [NCW][GMAX][kMergeStride]
+    wa.store_merge(mml + warp * GMAX * 2, macc + warp * GMAX * C::kMergeStride, C::kMergeStride, lane);
+    named_barrier_sync(1, NCW * 32);
+    const size_t orow0 = (size_t)s * p.num_q_heads + (size_t)h * g;
+    for (int idx = tid; idx < g * D; idx += NCW * 32) {
+        const int col = idx / D, d = idx - col * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, mml[(w * GMAX + col) * 2]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) {
+            const float mw = mml[(w * GMAX + col) * 2];
+            const float f = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
+            L += mml[(w * GMAX + col) * 2 + 1] * f;
+            O += macc[(w * GMAX + col) * C::kMergeStride + d] * f;
+        }
+        const float o = O / L;
+        if (npart == 1) {
+            out[(orow0 + col) * D + d] = o;
+        } else {
+            const size_t r = (orow0 + col) * p.max_parts + part;
+            p.ws_o[r * D + d] = o;
+            if (d == 0) {
+                p.ws_ml[r * 2 + 0] = M;
+                p.ws_ml[r * 2 + 1] = L;
+            }
+        }
+    }
+}
+
+// =====================================================================================
 // K2: log-sum-exp merge of a sequence's partitions, one CTA of D threads per
 // (query head, sequence):  M = max_p m_p;  w_p = l_p 2^(m_p - M);
 //   out = sum_p w_p o_p / sum_p w_p.
