@@ -1147,7 +1147,7 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="time the headline workload only")
     ap.add_argument("--partition-tokens", type=int, default=None)
     ap.add_argument("--dtype", choices=["bf16", "f32"], default=None,
-                    help="cache dtype (default: the workload's own); f32 runs the CUDA-core fp32 path")
+                    help="cache dtype (default: the workload's own); f32 runs the fp32 path")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
