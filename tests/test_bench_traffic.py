@@ -73,3 +73,22 @@ def test_a_change_outside_the_spans_keeps_the_fingerprint(monkeypatch, tmp_path)
     t2 = kern.read_text()
     kern.write_text(t2.replace("if (i == cnt - 1) break;", "if (i == cnt - 1) { break; }", 1))
     assert bench.kernel_source_sha256(k) != before
+
+
+def test_the_bench_names_kernels_the_sources_define():
+    """Every kernel name the bench line can report is a __global__ of the library."""
+    import re
+    from paged_kv_cache_177_gb300 import workloads as W
+    src = ""
+    for name in ("pkv_kernels.cuh", "pkv_prefill_tc.cuh"):
+        with open(bench.os.path.join(bench.ROOT, "paged_kv_cache_177_gb300", "csrc", name)) as f:
+            src += f.read()
+    defined = set(re.findall(r"__global__[^;{]*?\b(\w+_kernel)\s*\(", src, flags=re.S))
+    names = {"decode_bf16_persistent_kernel", "decode_bf16_kernel", "lse_reduce_kernel", "kv_append_kernel",
+             "move_blocks_kernel", "decode_bf16_cascade_kernel", "cascade_reduce_kernel", "prefill_tc_kernel",
+             "prefill_tc_units_kernel"}
+    names |= {bench.f32_kernel_name(W.spec(n, dtype="f32")) for n in W.SPECS}
+    names |= set(bench.KERNEL_SPANS)
+    assert names <= defined, names - defined
+    assert bench.f32_kernel_name(W.spec("long_context")) == "decode_f32_tc_kernel"   # 64 / 8 heads
+    assert bench.f32_kernel_name(W.spec("gqa8b")) == "decode_f32_staged_kernel"      # 32 / 8 heads
